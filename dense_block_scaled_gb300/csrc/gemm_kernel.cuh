@@ -1,0 +1,486 @@
+// gemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D[m][n] = alpha_eff * sum_k a(m,k) * b(n,k)      (A: M x K, B: N x K, K-major)
+//
+// FP32 accumulation in tensor memory, BF16 output.  Three operand formats:
+//   BF16  : kind::f16
+//   MXFP8 : kind::mxf8f6f4.block_scale.scale_vec::1X  (E4M3 values, E8M0 scale / 32 K)
+//   NVFP4 : kind::mxf4nvf4.block_scale.scale_vec::4X  (E2M1 values, UE4M3 scale / 16 K)
+// named by "ThunderKittens 2.0 GPU Kernel优化" (opening section: BF16/MXFP8/NVFP4
+// GEMMs) and recapped in "To Infinity and Beyond: ThunderKittens Now on NVIDIA Vera
+// Rubin NVL72!" (section "起点：NVIDIA HGX B200 GEMM").
+//
+// Structure (one CTA per SM, CG CTAs per cluster share one MMA when CG == 2):
+//   warp 0      TMA producer: A, B and scale tiles into a STAGES-deep ring, each
+//               stage gated by a full/empty mbarrier pair with explicit phase bits
+//               ("异步Tensor Core原理与实战", §3.2).
+//   warp 1      MMA issuer (pair leader only when CG == 2): waits for a stage,
+//               copies its scales to tensor memory with tcgen05.cp and issues the
+//               tcgen05.mma that read them from the same thread, so the copy and
+//               the MMA pipeline with no fence or barrier between them ("ThunderKittens
+//               2.0", §二 2.1).  No tcgen05.fence::after_thread_sync or
+//               fence.proxy.async sits between the stage wait and the MMA: the TMA
+//               data reaches the MMA through the complete_tx release / try_wait
+//               acquire of the same thread (§一 1.2).
+//   warp 2      tensor-memory allocation and release.
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator, release of the
+//               accumulator buffer, alpha scale, BF16 round-to-nearest-even, TMA
+//               store.  Accumulators are double buffered when tensor memory has
+//               room (BF16) so the next tile's MMAs overlap this drain (§二 2.2).
+//
+// Every wait is bounded: past the limit a role sets the device status word and
+// an abort flag, all roles leave their loops, in-flight copies and MMAs are
+// drained, tensor memory is freed and the kernel returns.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tkg {
+
+enum : int { FMT_BF16 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2 };
+enum : uint32_t { DEV_ERR_TIMEOUT = 1u };
+
+struct GemmParams {
+  int m, n, k;
+  int num_kstages;           // ceil(K / K-per-stage)
+  int tiles_m, tiles_n, num_tiles;
+  float alpha;
+  const float* ta;           // NVFP4 per-tensor scales (device, may be null)
+  const float* tb;
+  unsigned int* status;      // device status word (error bits)
+  unsigned long long timeout_ns;
+  int inject_stall;          // test hook: the MMA role waits on a barrier nothing arrives on
+};
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<FMT_BF16> {
+  static constexpr int kStageK = 64;      // K elements per stage (128 bytes of a row)
+  static constexpr int kMmaK = 16;        // K elements per MMA (32 bytes)
+  static constexpr int kSfAtoms = 0;      // 512-byte scale atoms per 128 rows per stage
+};
+template <>
+struct FmtTraits<FMT_MXFP8> {
+  static constexpr int kStageK = 128;
+  static constexpr int kMmaK = 32;
+  static constexpr int kSfAtoms = 1;      // 4 blocks of 32 = one atom per stage
+};
+template <>
+struct FmtTraits<FMT_NVFP4> {
+  static constexpr int kStageK = 256;
+  static constexpr int kMmaK = 64;
+  static constexpr int kSfAtoms = 4;      // 16 blocks of 16 = four atoms, one per MMA
+};
+
+// Instruction descriptor, kind::f16: D = F32, A = B = BF16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+// Instruction descriptor, block-scaled kinds.  fmt: 0 = E4M3 (mxf8f6f4), 1 = E2M1
+// (mxf4nvf4); scale: 1 = UE8M0, 0 = UE4M3; sf ids pick the byte of a scale word.
+__host__ __device__ constexpr uint32_t idesc_bs(int M, int N, uint32_t fmt, uint32_t scale_e8m0, uint32_t a_sf_id,
+                                                uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (fmt << 7) | (fmt << 10) | (uint32_t(N >> 3) << 17) | (scale_e8m0 << 23) |
+         (uint32_t(M >> 4) << 24) | (a_sf_id << 29);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Scale atom for tcgen05.cp 32x128b: 32 rows of 16 bytes, no swizzle, 8-row groups 128 B apart.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
+  return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t(128 >> 4) << 32) | (1ull << 46);
+}
+
+// Tile order: bands of kRasterGroup M-blocks walked N-fastest-within-band, so the
+// clusters running together share A rows and B columns in L2.
+constexpr int kRasterGroup = 8;
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  const int group_size = kRasterGroup * tiles_n;
+  const int group = t / group_size;
+  const int first_m = group * kRasterGroup;
+  const int gm = min(tiles_m - first_m, kRasterGroup);
+  const int r = t - group * group_size;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+template <int FMT, int CG, int BN, int STAGES, int ACC>
+struct GemmConfig {
+  using T = FmtTraits<FMT>;
+  static constexpr bool kScaled = FMT != FMT_BF16;
+  static constexpr int kThreads = 384;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCtaM = 128;                 // accumulator rows per CTA
+  static constexpr int kMmaM = 128 * CG;
+  static constexpr int kBRows = BN / CG;            // B rows loaded by each CTA
+  static constexpr int kRowBytes = 128;             // K bytes per stage row
+  static constexpr int kABytes = kCtaM * kRowBytes;
+  static constexpr int kBBytes = kBRows * kRowBytes;
+  static constexpr int kSfaBytes = T::kSfAtoms * 512;
+  static constexpr int kSfbBytes = (BN / 128) * T::kSfAtoms * 512;
+  static constexpr int kStageBytes = ((kABytes + kBBytes + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
+  static constexpr int kMmasPerStage = T::kStageK / T::kMmaK;
+  static constexpr int kEpiBufBytes = 32 * 64;      // 32 rows x 32 BF16
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
+  static constexpr int kNumBars = 2 * STAGES + 2 * ACC + 2;
+  static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + alignment slack
+  // bytes landing on the leader's full barrier per stage (all CTAs of the pair)
+  static constexpr uint32_t kTxBytes = uint32_t(CG * (kABytes + kBBytes + kSfaBytes + kSfbBytes));
+  // tensor memory
+  static constexpr int kAccCols = BN;
+  static constexpr int kSfaCols = T::kSfAtoms * 4;
+  static constexpr int kSfbCols = (BN / 128) * T::kSfAtoms * 4;
+  static constexpr int kSlotCols = kSfaCols + kSfbCols;
+  static constexpr int kScaleBase = ACC * kAccCols;
+  static constexpr int kTmemCols = 512;
+  static_assert(ACC * kAccCols + STAGES * kSlotCols <= kTmemCols, "tensor memory overflow");
+  static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
+  static_assert(kSmemBytes <= 232448, "shared memory overflow");
+  static constexpr uint32_t kIdescBase =
+      FMT == FMT_BF16 ? idesc_f16(kMmaM, BN)
+                      : idesc_bs(kMmaM, BN, FMT == FMT_NVFP4 ? 1u : 0u, FMT == FMT_MXFP8 ? 1u : 0u, 0u, 0u);
+};
+
+struct Ctl {
+  volatile int* abort_flag;   // this CTA's flag (shared memory)
+  uint32_t peer_abort;        // shared::cluster address of the peer's flag (CG == 2)
+  unsigned int* status;
+  unsigned long long timeout_ns;
+  int cg;
+};
+
+__device__ __forceinline__ void raise_abort(const Ctl& c) {
+  *c.abort_flag = 1;
+  if (c.cg == 2) ptx::st_shared_cluster_u32(c.peer_abort, 1u);
+  atomicOr(c.status, DEV_ERR_TIMEOUT);
+}
+
+// Bounded wait for the phase of parity `parity` of barrier `bar` to complete.
+// Returns false when the kernel is aborting (timeout here or elsewhere).
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
+#pragma unroll 1
+  for (int i = 0; i < 32; ++i) {
+    if (kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+  }
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      if (kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+    }
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer() - t0 > c.timeout_ns) {
+      raise_abort(c);
+      return false;
+    }
+  }
+}
+
+template <int FMT, int CG, int BN, int STAGES, int ACC>
+__global__ void __launch_bounds__(384, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+
+  // 1024-byte aligned carve-up (identical in both CTAs of a pair)
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  auto stage_a = [&](int s) { return base + uint32_t(s * C::kStageBytes); };
+  auto stage_b = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes); };
+  auto stage_sfa = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes); };
+  auto stage_sfb = [&](int s) {
+    return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes + C::kSfaBytes);
+  };
+  const uint32_t epi_base = base + uint32_t(STAGES * C::kStageBytes);
+  const uint32_t bars = base + uint32_t(C::kBarOffset);
+  auto full_bar = [&](int s) { return bars + uint32_t(8 * s); };
+  auto empty_bar = [&](int s) { return bars + uint32_t(8 * (STAGES + s)); };
+  auto accf_bar = [&](int a) { return bars + uint32_t(8 * (2 * STAGES + a)); };
+  auto acce_bar = [&](int a) { return bars + uint32_t(8 * (2 * STAGES + ACC + a)); };
+  const uint32_t drain_bar = bars + uint32_t(8 * (2 * STAGES + 2 * ACC));
+  const uint32_t never_bar = drain_bar + 8;
+  (void)gbase;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      ptx::mbar_init(accf_bar(a), 1);
+      ptx::mbar_init(acce_bar(a), C::kEpiWarps * CG);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    ptx::mbar_init(never_bar, 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmD);
+    if (C::kScaled) {
+      ptx::prefetch_tmap(&tmSFA);
+      ptx::prefetch_tmap(&tmSFB);
+    }
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc<CG>(ptx::smem_u32(&s_tmem_base), C::kTmemCols);
+    ptx::tmem_relinquish<CG>();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (CG == 2) ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  Ctl ctl;
+  ctl.abort_flag = &s_abort;
+  ctl.peer_abort = (CG == 2) ? ptx::map_to_rank(ptx::smem_u32(&s_abort), rank ^ 1u) : 0u;
+  ctl.status = p.status;
+  ctl.timeout_ns = p.timeout_ns;
+  ctl.cg = CG;
+
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
+
+  // ------------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      const uint64_t pol_a = ptx::policy_evict_last();
+      const uint64_t pol_b = ptx::policy_evict_normal();
+      // barrier the loads complete on: the pair leader's full barrier
+      const uint32_t lead_full0 = (CG == 2) ? ptx::map_to_rank(full_bar(0), 0) : full_bar(0);
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0;          // stages whose last arming is not yet known complete
+      uint32_t armed_par = 0;      // parity of that arming
+      bool ok = true;
+#pragma unroll 1
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        int mb, nb;
+        tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+        const int a_row = mb * C::kMmaM + int(rank) * C::kCtaM;
+        const int b_row = nb * BN + int(rank) * C::kBRows;
+#pragma unroll 1
+        for (int ks = 0; ks < p.num_kstages; ++ks) {
+          if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          armed &= ~(1u << stage);   // its previous load was consumed, hence complete
+          const uint32_t fb = lead_full0 + 8u * stage;
+          if (leader) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);   // TMA x coordinate (elements)
+          ptx::tma_load_2d<CG>(stage_a(stage), &tmA, kx, a_row, fb, pol_a);
+          ptx::tma_load_2d<CG>(stage_b(stage), &tmB, kx, b_row, fb, pol_b);
+          if constexpr (C::kScaled) {
+            const int atom0 = ks * FmtTraits<FMT>::kSfAtoms;
+            // SFA: this CTA's 128 rows = scale row-block (a_row / 128)
+            ptx::tma_load_3d<CG>(stage_sfa(stage), &tmSFA, 0, atom0, a_row / 128, fb, pol_a);
+            // SFB: the whole N tile, every CTA of the pair holds a copy
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(rb * FmtTraits<FMT>::kSfAtoms * 512), &tmSFB, 0,
+                                   atom0, nb * (BN / 128) + rb, fb, pol_b);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // drain: every armed stage completes once its bytes land
+#pragma unroll 1
+        for (int s = 0; s < STAGES; ++s) {
+          if (armed & (1u << s)) {
+            Ctl quiet = ctl;
+            int dummy = 0;
+            quiet.abort_flag = &dummy;   // keep waiting through the abort, still bounded
+            wait_bar<false>(full_bar(s), (armed_par >> s) & 1u, quiet);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+  // ------------------------------------------------------------------ MMA issuer
+  else if (warp == 1) {
+    if (leader && ptx::elect_one()) {
+      uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+      bool ok = true;
+      if (p.inject_stall) ok = wait_bar<false>(never_bar, 0u, ctl);
+      const uint16_t mask = (CG == 2) ? uint16_t(0x3) : uint16_t(0x1);
+#pragma unroll 1
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        if (!wait_bar<CG == 2>(acce_bar(acc), accph ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + uint32_t(acc * C::kAccCols);
+#pragma unroll 1
+        for (int ks = 0; ks < p.num_kstages; ++ks) {
+          if (!wait_bar<false>(full_bar(stage), phase, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t slot = tmem + uint32_t(C::kScaleBase + stage * C::kSlotCols);
+          if constexpr (C::kScaled) {
+            // scales -> tensor memory, same thread as the MMAs that read them
+#pragma unroll
+            for (int g = 0; g < FmtTraits<FMT>::kSfAtoms; ++g) {
+              ptx::tmem_cp_32x128b_x4<CG>(slot + uint32_t(4 * g), sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));
+#pragma unroll
+              for (int rb = 0; rb < BN / 128; ++rb)
+                ptx::tmem_cp_32x128b_x4<CG>(
+                    slot + uint32_t(C::kSfaCols + g * (BN / 128) * 4 + rb * 4),
+                    sdesc_sf(stage_sfb(stage) + uint32_t(rb * FmtTraits<FMT>::kSfAtoms * 512 + 512 * g)));
+            }
+          }
+          const uint64_t adesc = sdesc_sw128(stage_a(stage));
+          const uint64_t bdesc = sdesc_sw128(stage_b(stage));
+#pragma unroll
+          for (int j = 0; j < C::kMmasPerStage; ++j) {
+            const int k0 = ks * FmtTraits<FMT>::kStageK + j * FmtTraits<FMT>::kMmaK;
+            if (k0 < p.k) {
+              const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
+              const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
+              if constexpr (FMT == FMT_BF16) {
+                ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, accum);
+              } else if constexpr (FMT == FMT_MXFP8) {
+                // one atom per stage; MMA j reads byte j of each scale word
+                const uint32_t idesc = C::kIdescBase | (uint32_t(j) << 29) | (uint32_t(j) << 4);
+                ptx::mma_mxf8<CG>(d_tmem, adesc + koff, bdesc + koff, idesc, slot, slot + C::kSfaCols, accum);
+              } else {
+                // four atoms per stage; MMA j reads atom j (all four bytes)
+                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, slot + uint32_t(4 * j),
+                                  slot + uint32_t(C::kSfaCols + j * (BN / 128) * 4), accum);
+              }
+            }
+          }
+          ptx::tc_commit<CG>(empty_bar(stage), mask);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit<CG>(accf_bar(acc), mask);
+        if (++acc == ACC) {
+          acc = 0;
+          accph ^= 1u;
+        }
+      }
+      // every MMA this thread issued has finished before tensor memory goes away
+      ptx::tc_commit<CG>(drain_bar, uint16_t(1u << rank));
+      Ctl quiet = ctl;
+      int dummy = 0;
+      quiet.abort_flag = &dummy;
+      wait_bar<false>(drain_bar, 0u, quiet);
+    }
+    __syncwarp();
+  }
+  // ------------------------------------------------------------------ epilogue
+  else if (warp >= 4) {
+    const int e = warp - 4;
+    const int q = warp & 3;              // accumulator lane quadrant this warp may read
+    const int h = e >> 2;                // column half
+    const uint32_t my_buf0 = epi_base + uint32_t(e * 2 * C::kEpiBufBytes);
+    const uint32_t acce_lead0 = (CG == 2) ? ptx::map_to_rank(acce_bar(0), 0) : acce_bar(0);
+    float alpha = p.alpha;
+    if (p.ta) alpha = alpha * __ldg(p.ta);
+    if (p.tb) alpha = alpha * __ldg(p.tb);
+    uint32_t acc = 0, accph = 0;
+#pragma unroll 1
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      uint32_t ok = 0;
+      if (lane == 0) ok = wait_bar<false>(accf_bar(acc), accph, ctl) ? 1u : 0u;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      constexpr int kChunks = BN / 2 / 32;
+      uint32_t v[kChunks][32];
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v[c]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acce_lead0 + 8u * acc);
+      if (++acc == ACC) {
+        acc = 0;
+        accph ^= 1u;
+      }
+      const int row0 = mb * C::kMmaM + int(rank) * C::kCtaM + q * 32;
+      const int col0 = nb * BN + h * (BN / 2);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t buf = my_buf0 + uint32_t((c & 1) * C::kEpiBufBytes);
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t row_addr = buf + uint32_t(lane * 64);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float lo = __uint_as_float(v[c][8 * j + 2 * x]) * alpha;
+            const float hi = __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha;
+            w[x] = ptx::pack_bf16x2(lo, hi);
+          }
+          const uint32_t chunk = uint32_t(j) ^ ((uint32_t(lane) >> 1) & 3u);   // 64-byte swizzle
+          ptx::st_shared_v4(row_addr + chunk * 16u, w[0], w[1], w[2], w[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmD, buf, col0 + c * 32, row0);
+          ptx::bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (s_abort && threadIdx.x == 0) {
+    // let any copy still in flight land before this CTA's shared memory is released
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 50000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (CG == 2) ptx::cluster_sync();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc<CG>(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace tkg

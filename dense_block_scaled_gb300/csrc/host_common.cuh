@@ -1,0 +1,161 @@
+// host_common.cuh -- host-side plumbing shared by the launchers: tensor-map
+// encoding through the driver entry point, per-device state (status word, SM
+// count), process-wide options, and the persistent cluster launch.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/tkg_gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace tkg {
+
+struct Problem {
+  int m, n, k;
+  const void* A;
+  const void* B;
+  const void* sfa;
+  const void* sfb;
+  const float* ta;
+  const float* tb;
+  void* D;
+  float alpha;
+};
+
+// ---- options and per-device state (tkg_api.cu)
+int option(tkg_option o);
+tkg_status device_status_word(unsigned int** out);   // lazily allocated per device
+tkg_status device_sm_count(int* out);
+
+// ---- tensor maps (tkg_api.cu)
+tkg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz);
+tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                     uint32_t box2);
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Launch one instantiation of the persistent GEMM.
+template <int FMT, int CG, int BN, int STAGES, int ACC>
+tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC>;
+  using T = FmtTraits<FMT>;
+  auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC>;
+  // Request at least just over half an SM's shared memory so that no two CTAs
+  // ever share an SM: each allocates all 512 tensor-memory columns.
+  constexpr int kLaunchSmem = C::kSmemBytes > 118784 ? C::kSmemBytes : 118784;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TKG_ERR_CUDA;
+  static bool attr_set[64] = {};   // per instantiation and device (idempotent if two threads race)
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLaunchSmem) != cudaSuccess)
+      return TKG_ERR_CUDA;
+    if (CG == 2 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      cudaGetLastError();
+    }
+    attr_set[dev] = true;
+  }
+
+  // operand tensor maps: 128-byte K rows per stage, 128-byte swizzle
+  CUtensorMap tmA, tmB, tmSFA, tmSFB, tmD;
+  const bool bf16 = FMT == FMT_BF16;
+  const CUtensorMapDataType vt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t kdim = FMT == FMT_NVFP4 ? uint64_t(pr.k) / 2 : uint64_t(pr.k);   // elements along dim0
+  const uint64_t row_bytes = FMT == FMT_BF16 ? uint64_t(pr.k) * 2 : kdim;
+  const uint32_t boxk = bf16 ? 64 : 128;
+  tkg_status st;
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+    return st;
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+    return st;
+  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
+    return st;
+  if constexpr (C::kScaled) {
+    const int bs = FMT == FMT_MXFP8 ? 32 : 16;
+    const int ka = ceil_div(ceil_div(pr.k, bs), 4);   // 512-byte atoms per 128-row block
+    if ((st = encode_3d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfa, 128, ka, ceil_div(pr.m, 128), 512,
+                        uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
+      return st;
+    if ((st = encode_3d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfb, 128, ka, ceil_div(pr.n, 128), 512,
+                        uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
+      return st;
+  } else {
+    tmSFA = tmD;
+    tmSFB = tmD;
+  }
+
+  GemmParams p;
+  p.m = pr.m;
+  p.n = pr.n;
+  p.k = pr.k;
+  p.num_kstages = ceil_div(pr.k, T::kStageK);
+  p.tiles_m = ceil_div(pr.m, C::kMmaM);
+  p.tiles_n = ceil_div(pr.n, BN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.alpha = pr.alpha;
+  p.ta = pr.ta;
+  p.tb = pr.tb;
+  if ((st = device_status_word(&p.status)) != TKG_OK) return st;
+  const int tmo = option(TKG_OPT_TIMEOUT_MS);
+  p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
+  p.inject_stall = option(TKG_OPT_INJECT_STALL);
+
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != TKG_OK) return st;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kLaunchSmem;
+  cfg.stream = stream;
+  int nattr = 0;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    nattr = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+
+  // persistent grid: as many clusters as can be resident at once, no more than tiles
+  static int max_clusters_dev[64] = {};
+  int& max_clusters = max_clusters_dev[dev];
+  if (max_clusters == 0) {
+    if (CG == 2) {
+      cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc <= 0) {
+        cudaGetLastError();
+        nc = sms / 2;
+      }
+      max_clusters = nc;
+    } else {
+      max_clusters = sms;
+    }
+  }
+  int clusters = max_clusters < p.num_tiles ? max_clusters : p.num_tiles;
+  const int cap = option(TKG_OPT_MAX_CLUSTERS);
+  if (cap > 0 && clusters > cap) clusters = cap;
+  cfg.gridDim = dim3(clusters * CG, 1, 1);
+
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  return TKG_OK;
+}
+
+tkg_status launch_bf16(const Problem& pr, cudaStream_t s);
+tkg_status launch_mxfp8(const Problem& pr, cudaStream_t s);
+tkg_status launch_nvfp4(const Problem& pr, cudaStream_t s);
+
+}  // namespace tkg

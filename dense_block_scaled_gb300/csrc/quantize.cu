@@ -1,0 +1,231 @@
+// quantize.cu -- FP32 -> MXFP8 / NVFP4 quantisers and the row-major -> tiled
+// scale-layout conversion.  All HBM-bound: coalesced 16-byte loads, grid sized
+// to a multiple of the SM count, grid-stride loops.
+//
+// Quantisation rules are those of the workload definition (MXFP8: E8M0 scale
+// 2^ceil(log2(amax/448)) per 1x32 block, E4M3 RNE saturating; NVFP4: FP32
+// tensor scale amax/(6*448), E4M3 block scale blockamax/(6*tensor scale) per
+// 1x16 block, E2M1 RNE), for the MXFP8/NVFP4 formats of "ThunderKittens 2.0
+// GPU Kernel优化" (table of updates).  Every FP32 step is one IEEE operation
+// with round-to-nearest (explicit __f*_rn intrinsics, never contracted).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "host_common.cuh"
+
+namespace tkg {
+
+// Byte offset of scale (r, kb) in the tiled layout (include/tkg_gemm.h).
+__device__ __forceinline__ size_t sf_tiled_offset(int r, int kb, int ka) {
+  return (size_t(r >> 7) * size_t(ka) + size_t(kb >> 2)) * 512u + size_t(r & 31) * 16u +
+         size_t((r & 127) >> 5) * 4u + size_t(kb & 3);
+}
+
+// Two FP32 -> E4M3 (RNE, saturating); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two FP32 -> E2M1 (RNE, saturating); `lo` lands in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// Value of a non-negative E4M3 code (bias 7, 3 mantissa bits, subnormals m * 2^-9).
+__device__ __forceinline__ float e4m3_value(uint32_t s) {
+  const uint32_t e = (s >> 3) & 0xFu, m = s & 7u;
+  if (e == 0) return __fmul_rn(float(m), 1.0f / 512.0f);
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// MXFP8 scale exponent: smallest e with 448 * 2^e >= amax, clamped to [-127, 127].
+// With amax = M * 2^E (M in [1, 2)), 448 = 1.75 * 2^8, that is
+// e = E - 8 + (M > 1.75); subnormal or zero amax gives -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  const int eb = int((u >> 23) & 0xFFu);
+  if (eb == 0) return -127;
+  int e = (eb - 127) - 8 + (((u & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// One warp = four 32-element blocks per pass; lane l takes 4 consecutive elements.
+__global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kblk, const float* __restrict__ X,
+                                                          uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
+                                                          int ka) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long passes = (nblk + 3) / 4;
+  for (long long w = warp0; w < passes; w += nwarps) {
+    const long long b = w * 4 + (lane >> 3);
+    const bool valid = b < nblk;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) x = __ldcs(reinterpret_cast<const float4*>(X + b * 32 + 4 * (lane & 7)));
+    float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    const int e = mx_exponent(a);
+    const float inv = __uint_as_float(uint32_t(127 - e) << 23);   // 2^-e, a normal float for e in [-127, 120]
+    if (valid) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x.z, inv), __fmul_rn(x.w, inv));
+      *reinterpret_cast<uint32_t*>(Q + b * 32 + 4 * (lane & 7)) = lo | (hi << 16);
+      if ((lane & 7) == 0) {
+        const int r = int(b / kblk), kb = int(b % kblk);
+        SF[sf_tiled_offset(r, kb, ka)] = uint8_t(e + 127);
+      }
+    }
+  }
+}
+
+// amax over the whole tensor, as the bits of a non-negative float (monotone as unsigned).
+__global__ void __launch_bounds__(256) amax_kernel(long long n4, const float* __restrict__ X,
+                                                   unsigned int* __restrict__ out) {
+  float a = 0.f;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(X) + i);
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+  }
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float b = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 4; o > 0; o >>= 1) b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    if (threadIdx.x == 0) atomicMax(out, __float_as_uint(b));
+  }
+}
+
+// t = amax / (6 * 448), in place.
+__global__ void tensor_scale_kernel(unsigned int* __restrict__ word) {
+  const float amax = __uint_as_float(*word);
+  *reinterpret_cast<float*>(word) = __fdiv_rn(amax, 2688.0f);
+}
+
+// One warp = eight 16-element blocks per pass; lane l takes 4 consecutive elements.
+__global__ void __launch_bounds__(256) quant_nvfp4_kernel(long long nblk, int kblk, const float* __restrict__ X,
+                                                          uint8_t* __restrict__ Q, uint8_t* __restrict__ SF, int ka,
+                                                          const float* __restrict__ tptr) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long passes = (nblk + 7) / 8;
+  const float t = __ldg(tptr);
+  const float d = __fmul_rn(6.0f, t);
+  for (long long w = warp0; w < passes; w += nwarps) {
+    const long long b = w * 8 + (lane >> 2);
+    const bool valid = b < nblk;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) x = __ldcs(reinterpret_cast<const float4*>(X + b * 16 + 4 * (lane & 3)));
+    float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    uint32_t s = 0;
+    float den = 0.f;
+    if (t > 0.f) {
+      s = cvt_e4m3x2(__fdiv_rn(a, d), 0.f) & 0xFFu;
+      den = __fmul_rn(e4m3_value(s), t);
+    }
+    if (valid) {
+      uint32_t packed = 0;
+      if (den > 0.f) {
+        const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x.x, den), __fdiv_rn(x.y, den));
+        const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x.z, den), __fdiv_rn(x.w, den));
+        packed = lo | (hi << 8);
+      }
+      *reinterpret_cast<uint16_t*>(Q + b * 8 + 2 * (lane & 3)) = uint16_t(packed);
+      if ((lane & 3) == 0) {
+        const int r = int(b / kblk), kb = int(b % kblk);
+        SF[sf_tiled_offset(r, kb, ka)] = uint8_t(s);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) scales_to_tiled_kernel(int rows, int kblocks, const uint8_t* __restrict__ src,
+                                                              int ld, uint8_t* __restrict__ dst, int ka) {
+  const long long n = (long long)rows * kblocks;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int r = int(i / kblocks), kb = int(i % kblocks);
+    dst[sf_tiled_offset(r, kb, ka)] = src[(size_t)r * ld + kb];
+  }
+}
+
+static int grid_for(long long work_items, int per_block) {
+  int sms = 148;
+  device_sm_count(&sms);
+  long long want = (work_items + per_block - 1) / per_block;
+  long long cap = (long long)sms * 8;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  return int(want);
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace tkg
+
+using namespace tkg;
+
+extern "C" {
+
+tkg_status tkg_quantize_mxfp8(int rows, int k, const float* X, void* Q, void* sf, cudaStream_t stream) {
+  if (rows < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (rows == 0 || k == 0) return TKG_OK;
+  if (!X || !Q || !sf) return TKG_ERR_INVALID_ARG;
+  if (k % 32 != 0 || !aligned(X, 16) || !aligned(Q, 16) || !aligned(sf, 16)) return TKG_ERR_ALIGNMENT;
+  const int kblk = k / 32, ka = (kblk + 3) / 4;
+  if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 32), stream) != cudaSuccess) return TKG_ERR_CUDA;
+  const long long nblk = (long long)rows * kblk;
+  quant_mxfp8_kernel<<<grid_for((nblk + 3) / 4 * 32, 256), 256, 0, stream>>>(
+      nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka);
+  return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
+}
+
+tkg_status tkg_quantize_nvfp4(int rows, int k, const float* X, void* Q, void* sf, float* tensor_scale,
+                              cudaStream_t stream) {
+  if (rows < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (!tensor_scale) return TKG_ERR_INVALID_ARG;
+  if (!aligned(tensor_scale, 4)) return TKG_ERR_ALIGNMENT;
+  if (cudaMemsetAsync(tensor_scale, 0, sizeof(float), stream) != cudaSuccess) return TKG_ERR_CUDA;
+  if (rows == 0 || k == 0) return TKG_OK;
+  if (!X || !Q || !sf) return TKG_ERR_INVALID_ARG;
+  if (k % 32 != 0 || !aligned(X, 16) || !aligned(Q, 16) || !aligned(sf, 16)) return TKG_ERR_ALIGNMENT;
+  const int kblk = k / 16, ka = (kblk + 3) / 4;
+  if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 16), stream) != cudaSuccess) return TKG_ERR_CUDA;
+  unsigned int* word = reinterpret_cast<unsigned int*>(tensor_scale);
+  const long long n4 = (long long)rows * k / 4;
+  amax_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(n4, X, word);
+  tensor_scale_kernel<<<1, 1, 0, stream>>>(word);
+  const long long nblk = (long long)rows * kblk;
+  quant_nvfp4_kernel<<<grid_for((nblk + 7) / 8 * 32, 256), 256, 0, stream>>>(
+      nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka, tensor_scale);
+  return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
+}
+
+tkg_status tkg_scales_to_tiled(int rows, int kblocks, const void* src, int ld, void* dst, cudaStream_t stream) {
+  if (rows < 0 || kblocks < 0 || ld < kblocks) return TKG_ERR_INVALID_ARG;
+  if (rows == 0 || kblocks == 0) return TKG_OK;
+  if (!src || !dst) return TKG_ERR_INVALID_ARG;
+  const int ka = (kblocks + 3) / 4;
+  const size_t bytes = size_t((rows + 127) / 128) * 128 * size_t(ka) * 4;
+  if (cudaMemsetAsync(dst, 0, bytes, stream) != cudaSuccess) return TKG_ERR_CUDA;
+  const long long n = (long long)rows * kblocks;
+  scales_to_tiled_kernel<<<grid_for(n, 256), 256, 0, stream>>>(rows, kblocks, static_cast<const uint8_t*>(src), ld,
+                                                               static_cast<uint8_t*>(dst), ka);
+  return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
+}
+
+}  // extern "C"

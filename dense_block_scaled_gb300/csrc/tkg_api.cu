@@ -1,0 +1,212 @@
+// tkg_api.cu -- the C ABI (include/tkg_gemm.h): argument checks, per-device
+// state, options, tensor-map encoding, dispatch to the format launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "host_common.cuh"
+
+namespace tkg {
+
+// ------------------------------------------------------------------ options
+static std::atomic<int> g_opts[8];
+
+int option(tkg_option o) {
+  const int i = int(o);
+  return (i > 0 && i < 8) ? g_opts[i].load(std::memory_order_relaxed) : 0;
+}
+
+// ------------------------------------------------------------------ per-device state
+static std::mutex g_dev_mu;
+static unsigned int* g_status[64] = {};
+static int g_sms[64] = {};
+
+static int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return (dev >= 0 && dev < 64) ? dev : -1;
+}
+
+tkg_status device_status_word(unsigned int** out) {
+  const int dev = current_device();
+  if (dev < 0) return TKG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_status[dev]) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) return TKG_ERR_CUDA;
+    if (cudaMemset(p, 0, 256) != cudaSuccess) return TKG_ERR_CUDA;
+    g_status[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status[dev];
+  return TKG_OK;
+}
+
+tkg_status device_sm_count(int* out) {
+  const int dev = current_device();
+  if (dev < 0) return TKG_ERR_CUDA;
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return TKG_ERR_CUDA;
+    g_sms[dev] = n;
+  }
+  *out = g_sms[dev];
+  return TKG_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+tkg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TKG_ERR_CUDA;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+}
+
+tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                     uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TKG_ERR_CUDA;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks; returns TKG_OK and sets *empty when there is nothing to launch.
+static tkg_status check_common(int m, int n, int k, const void* A, const void* B, void* D, int k_multiple,
+                               bool* empty, cudaStream_t stream) {
+  *empty = false;
+  if (m < 0 || n < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) {
+    *empty = true;
+    return TKG_OK;
+  }
+  if (!D) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(D) || (n % 8) != 0) return TKG_ERR_ALIGNMENT;
+  if (k == 0) {   // empty sum: D = 0
+    *empty = true;
+    return cudaMemsetAsync(D, 0, size_t(m) * size_t(n) * 2, stream) == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
+  }
+  if (!A || !B) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || (k % k_multiple) != 0) return TKG_ERR_ALIGNMENT;
+  return TKG_OK;
+}
+
+}  // namespace tkg
+
+using namespace tkg;
+
+extern "C" {
+
+tkg_status tkg_gemm_bf16(int m, int n, int k, const void* A, const void* B, void* D, float alpha,
+                         cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_common(m, n, k, A, B, D, 8, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  Problem pr{m, n, k, A, B, nullptr, nullptr, nullptr, nullptr, D, alpha};
+  return launch_bf16(pr, stream);
+}
+
+tkg_status tkg_gemm_mxfp8(int m, int n, int k, const void* A, const void* B, const void* sfa, const void* sfb,
+                          void* D, float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_common(m, n, k, A, B, D, 32, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  Problem pr{m, n, k, A, B, sfa, sfb, nullptr, nullptr, D, alpha};
+  return launch_mxfp8(pr, stream);
+}
+
+tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void* A, const void* B, const void* sfa, const void* sfb,
+                          const float* tensor_scale_a, const float* tensor_scale_b, void* D, float alpha,
+                          cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_common(m, n, k, A, B, D, 32, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  if ((tensor_scale_a && (reinterpret_cast<uintptr_t>(tensor_scale_a) & 3u)) ||
+      (tensor_scale_b && (reinterpret_cast<uintptr_t>(tensor_scale_b) & 3u)))
+    return TKG_ERR_ALIGNMENT;
+  Problem pr{m, n, k, A, B, sfa, sfb, tensor_scale_a, tensor_scale_b, D, alpha};
+  return launch_nvfp4(pr, stream);
+}
+
+tkg_status tkg_get_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+  unsigned int* w = nullptr;
+  tkg_status st = device_status_word(&w);
+  if (st != TKG_OK) return st;
+  unsigned int h = 0;
+  if (cudaMemcpyAsync(&h, w, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return TKG_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+  if (h == 0) return TKG_OK;
+  if (cudaMemsetAsync(w, 0, sizeof h, stream) != cudaSuccess) return TKG_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+  return (h & DEV_ERR_TIMEOUT) ? TKG_ERR_TIMEOUT : TKG_ERR_CUDA;
+}
+
+const char* tkg_status_string(tkg_status s) {
+  switch (s) {
+    case TKG_OK: return "ok";
+    case TKG_ERR_INVALID_ARG: return "invalid argument";
+    case TKG_ERR_ALIGNMENT: return "misaligned pointer or row pitch";
+    case TKG_ERR_UNSUPPORTED: return "unsupported shape";
+    case TKG_ERR_CUDA: return "CUDA error";
+    case TKG_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t tkg_scale_bytes(int rows, int k, int block) {
+  if (rows < 0 || k < 0 || (block != 16 && block != 32)) return 0;
+  const size_t rpad = size_t(ceil_div(rows, 128)) * 128;
+  const size_t kbpad = size_t(ceil_div(ceil_div(k, block), 4)) * 4;
+  return rpad * kbpad;
+}
+
+tkg_status tkg_set_option(tkg_option o, int value) {
+  const int i = int(o);
+  if (i <= 0 || i >= 8 || value < 0) return TKG_ERR_INVALID_ARG;
+  if (o == TKG_OPT_CTA_GROUP && value > 2) return TKG_ERR_INVALID_ARG;
+  g_opts[i].store(value, std::memory_order_relaxed);
+  return TKG_OK;
+}
+
+int tkg_get_option(tkg_option o) { return option(o); }
+
+}  // extern "C"

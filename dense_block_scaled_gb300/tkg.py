@@ -1,0 +1,164 @@
+"""ctypes binding of libtkg.so (C ABI in include/tkg_gemm.h).
+
+Argument marshalling only: every entry point forwards device pointers, sizes
+and a CUDA stream handle to the library; all arithmetic runs in the library's
+CUDA kernels.  The library is built in-tree (``python -m
+dense_block_scaled_gb300.build``); if it is missing or fails to load, every
+call raises -- there is no fallback path.
+
+Helpers accept torch tensors only as carriers of device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libtkg.so")
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
+OPT_CTA_GROUP, OPT_SINGLE_STAGE, OPT_TIMEOUT_MS, OPT_INJECT_STALL, OPT_MAX_CLUSTERS = 1, 2, 3, 4, 5
+
+EXPORTS = [
+    "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",
+    "tkg_scale_bytes", "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
+    "tkg_set_option", "tkg_get_option",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TkgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libtkg.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m dense_block_scaled_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            i, vp, f, st = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+            lib.tkg_gemm_bf16.argtypes = [i, i, i, vp, vp, vp, f, vp]
+            lib.tkg_gemm_mxfp8.argtypes = [i, i, i, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_gemm_nvfp4.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_get_device_status.argtypes = [vp]
+            lib.tkg_status_string.argtypes = [st]
+            lib.tkg_status_string.restype = ctypes.c_char_p
+            lib.tkg_scale_bytes.argtypes = [i, i, i]
+            lib.tkg_scale_bytes.restype = ctypes.c_size_t
+            lib.tkg_scales_to_tiled.argtypes = [i, i, vp, i, vp, vp]
+            lib.tkg_quantize_mxfp8.argtypes = [i, i, vp, vp, vp, vp]
+            lib.tkg_quantize_nvfp4.argtypes = [i, i, vp, vp, vp, vp, vp]
+            lib.tkg_set_option.argtypes = [i, i]
+            lib.tkg_get_option.argtypes = [i]
+            for name in ("tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status",
+                         "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4", "tkg_set_option",
+                         "tkg_get_option"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().tkg_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise TkgError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- raw C calls (pointers)
+
+def gemm_bf16_raw(m, n, k, A, B, D, alpha, stream) -> int:
+    return load().tkg_gemm_bf16(m, n, k, A, B, D, ctypes.c_float(alpha), stream)
+
+
+def gemm_mxfp8_raw(m, n, k, A, B, sfa, sfb, D, alpha, stream) -> int:
+    return load().tkg_gemm_mxfp8(m, n, k, A, B, sfa, sfb, D, ctypes.c_float(alpha), stream)
+
+
+def gemm_nvfp4_raw(m, n, k, A, B, sfa, sfb, ta, tb, D, alpha, stream) -> int:
+    return load().tkg_gemm_nvfp4(m, n, k, A, B, sfa, sfb, ta, tb, D, ctypes.c_float(alpha), stream)
+
+
+# ---------------------------------------------------------------- tensor helpers
+
+def gemm_bf16(A, B, D, alpha: float = 1.0, stream=None) -> None:
+    """D (m x n bf16) = alpha * A (m x k bf16) @ B (n x k bf16)^T."""
+    m, k = A.shape
+    n = B.shape[0]
+    _check(gemm_bf16_raw(m, n, k, _ptr(A), _ptr(B), _ptr(D), alpha, _stream(stream)), "tkg_gemm_bf16")
+
+
+def gemm_mxfp8(A, B, sfa, sfb, D, alpha: float = 1.0, stream=None) -> None:
+    """A (m x k uint8 E4M3), B (n x k), tiled E8M0 scales sfa / sfb (uint8)."""
+    m, k = A.shape
+    n = B.shape[0]
+    _check(gemm_mxfp8_raw(m, n, k, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(D), alpha, _stream(stream)),
+           "tkg_gemm_mxfp8")
+
+
+def gemm_nvfp4(A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, tb=None, stream=None) -> None:
+    """A (m x k/2 uint8, packed E2M1), B (n x k/2), tiled UE4M3 scales, FP32 per-tensor scales ta / tb (device)."""
+    m, kh = A.shape
+    n = B.shape[0]
+    _check(gemm_nvfp4_raw(m, n, 2 * kh, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
+                          alpha, _stream(stream)), "tkg_gemm_nvfp4")
+
+
+def scale_bytes(rows: int, k: int, block: int) -> int:
+    return int(load().tkg_scale_bytes(rows, k, block))
+
+
+def scales_to_tiled(src, dst, kblocks: int | None = None, stream=None) -> None:
+    rows, ld = src.shape
+    kb = ld if kblocks is None else kblocks
+    _check(load().tkg_scales_to_tiled(rows, kb, _ptr(src), ld, _ptr(dst), _stream(stream)), "tkg_scales_to_tiled")
+
+
+def quantize_mxfp8(X, Q, sf, stream=None) -> None:
+    rows, k = X.shape
+    _check(load().tkg_quantize_mxfp8(rows, k, _ptr(X), _ptr(Q), _ptr(sf), _stream(stream)), "tkg_quantize_mxfp8")
+
+
+def quantize_nvfp4(X, Q, sf, tensor_scale, stream=None) -> None:
+    rows, k = X.shape
+    _check(load().tkg_quantize_nvfp4(rows, k, _ptr(X), _ptr(Q), _ptr(sf), _ptr(tensor_scale), _stream(stream)),
+           "tkg_quantize_nvfp4")
+
+
+def device_status(stream=None) -> int:
+    return int(load().tkg_get_device_status(_stream(stream)))
+
+
+def set_option(option: int, value: int) -> None:
+    _check(load().tkg_set_option(option, value), "tkg_set_option")
+
+
+def get_option(option: int) -> int:
+    return int(load().tkg_get_option(option))

@@ -1,0 +1,143 @@
+/*
+ * tkg_gemm.h -- C ABI of libtkg.so: dense and block-scaled GEMM on one GB300
+ * (sm_103a), plus the quantisers and the scale-layout conversion that feed it.
+ *
+ *   D = alpha_eff * A * B^T
+ *
+ * A is M x K and B is N x K, both row-major ("K-major", K contiguous); D is
+ * M x N row-major BF16.  Products are accumulated in FP32 on the tensor cores;
+ * D is alpha_eff * acc rounded to nearest-even BF16.  The three operand formats
+ * are the BF16 / MXFP8 / NVFP4 GEMMs of "ThunderKittens 2.0 GPU Kernel优化"
+ * (yunpan.plus write-up of the HazyResearch TK 2.0 release, opening section and
+ * its table of updates); the pages name the formats, these declarations fix
+ * their layouts.
+ *
+ * Conventions for every entry point below:
+ *  - Pointers named A, B, D, X, Q, sfa, sfb, sf, src, dst are DEVICE pointers
+ *    owned by the caller; the library keeps no reference after the call.
+ *  - Calls are asynchronous on `stream` and return after enqueueing work.
+ *    Device-side failures (a bounded wait that ran out) are reported by
+ *    tkg_get_device_status().
+ *  - Arguments are checked before anything is launched: negative sizes or a
+ *    null pointer give TKG_ERR_INVALID_ARG, a base address or row pitch that
+ *    is not a multiple of 16 bytes gives TKG_ERR_ALIGNMENT, shapes the kernels
+ *    do not handle give TKG_ERR_UNSUPPORTED.  A CUDA error while enqueueing
+ *    gives TKG_ERR_CUDA.  There is no CPU fallback.
+ *  - m == 0 or n == 0 is an empty GEMM (nothing is written); k == 0 writes
+ *    zeros to D (an empty sum).
+ *
+ * Block-scaled scale factors use the TILED layout (tkg_scale_bytes): for a
+ * matrix with R rows and KB = ceil(K / bs) scale blocks per row (bs = 32 for
+ * MXFP8, 16 for NVFP4), scale (r, kb) is the byte at
+ *
+ *     ((r / 128) * KA + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4
+ *
+ * with KA = ceil(KB / 4).  Each 512-byte atom holds 128 rows x 4 blocks in the
+ * order the tensor cores read scales from tensor memory, so the kernel moves
+ * atoms from HBM to shared memory to tensor memory without rearranging bytes.
+ * Rows beyond R and blocks beyond KB are padding: padding blocks inside a row
+ * must hold a finite scale code (zero is recommended; the quantisers and
+ * tkg_scales_to_tiled write zeros).  tkg_scales_to_tiled() converts a
+ * row-major scale matrix into this layout.
+ */
+#ifndef TKG_GEMM_H
+#define TKG_GEMM_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TKG_OK = 0,
+  TKG_ERR_INVALID_ARG = 1,
+  TKG_ERR_ALIGNMENT = 2,
+  TKG_ERR_UNSUPPORTED = 3,
+  TKG_ERR_CUDA = 4,
+  TKG_ERR_TIMEOUT = 5
+} tkg_status;
+
+/* BF16 GEMM ("ThunderKittens 2.0", opening section: BF16 GEMM on B200).
+ * A: m x k bfloat16, B: n x k bfloat16, D: m x n bfloat16, all row-major.
+ * Requires k % 8 == 0 and n % 8 == 0 (16-byte row pitches) and 16-byte
+ * aligned A, B, D.  D = bf16_rn(alpha * sum_k A[i][k] * B[j][k]). */
+tkg_status tkg_gemm_bf16(int m, int n, int k, const void *A, const void *B, void *D, float alpha,
+                         cudaStream_t stream);
+
+/* MXFP8 GEMM ("ThunderKittens 2.0", table of updates: MXFP8 support).
+ * A: m x k bytes (FP8 E4M3), B: n x k bytes (E4M3), sfa / sfb: E8M0 scale
+ * codes (2^(c-127)), one per 1 x 32 block along K, tiled layout (bs = 32),
+ * tkg_scale_bytes(m, k, 32) / tkg_scale_bytes(n, k, 32) bytes.
+ * Requires k % 32 == 0, n % 8 == 0, 16-byte aligned pointers.
+ * D[i][j] = bf16_rn(alpha * sum_k a_ik * sa(i, k/32) * b_jk * sb(j, k/32)). */
+tkg_status tkg_gemm_mxfp8(int m, int n, int k, const void *A, const void *B, const void *sfa, const void *sfb,
+                          void *D, float alpha, cudaStream_t stream);
+
+/* NVFP4 GEMM ("ThunderKittens 2.0", table of updates: NVFP4 support; §二 2.1
+ * on its scale path).  A: m x k/2 bytes, B: n x k/2 bytes, two FP4 E2M1 codes
+ * per byte, element 2j in the low nibble of byte j.  sfa / sfb: UE4M3 scale
+ * codes, one per 1 x 16 block along K, tiled layout (bs = 16).
+ * tensor_scale_a / tensor_scale_b: device pointers to the FP32 per-tensor
+ * scales (either may be NULL, meaning 1.0).  The kernel forms
+ * alpha_eff = fp32(fp32(alpha * tA) * tB).  Requires k % 32 == 0, n % 8 == 0.
+ * D[i][j] = bf16_rn(alpha_eff * sum_k a_ik * sa(i, k/16) * b_jk * sb(j, k/16)). */
+tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void *A, const void *B, const void *sfa, const void *sfb,
+                          const float *tensor_scale_a, const float *tensor_scale_b, void *D, float alpha,
+                          cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: TKG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call (its output is then unspecified), TKG_ERR_CUDA on a CUDA error,
+ * TKG_OK otherwise. */
+tkg_status tkg_get_device_status(cudaStream_t stream);
+
+/* Static string naming a status code. */
+const char *tkg_status_string(tkg_status status);
+
+/* Bytes of a tiled scale buffer for `rows` rows, K = k, block size `block`
+ * (32 for MXFP8, 16 for NVFP4): ceil(rows/128)*128 * ceil(ceil(k/block)/4)*4.
+ * Returns 0 for invalid arguments. */
+size_t tkg_scale_bytes(int rows, int k, int block);
+
+/* Row-major scale matrix (rows x kblocks codes, row pitch ld bytes) -> tiled
+ * layout in dst (tkg_scale_bytes(rows, kblocks * block, block) bytes; padding
+ * written as zero).  One GPU kernel, byte exact. */
+tkg_status tkg_scales_to_tiled(int rows, int kblocks, const void *src, int ld, void *dst, cudaStream_t stream);
+
+/* MXFP8 quantiser, following the workload rule: per 1 x 32 block of each row
+ * of X (rows x k FP32, row-major), amax = max |x|, scale exponent
+ * e = ceil(log2(amax / 448)) (smallest e with 448 * 2^e >= amax, clamped to
+ * [-127, 127]; an all-zero block gets -127), code = e + 127, and
+ * q = E4M3 round-to-nearest-even, saturating, of x * 2^-e (FP32).
+ * Q: rows x k bytes; sf: tiled layout (bs = 32).  Requires k % 32 == 0. */
+tkg_status tkg_quantize_mxfp8(int rows, int k, const float *X, void *Q, void *sf, cudaStream_t stream);
+
+/* NVFP4 quantiser, following the workload rule, every step one FP32 IEEE
+ * operation in the order written:
+ *   t = amax(X) / 2688 (= 6 * 448);  per 1 x 16 block:
+ *   s = E4M3_rne_sat(blockamax / (6 * t));  q = E2M1_rne_sat(x / (dec(s) * t)).
+ * t == 0 or dec(s) == 0 gives q = 0.  Q: rows x k/2 bytes (low nibble first),
+ * sf: tiled layout (bs = 16), tensor_scale: one FP32 written with t.
+ * Requires k % 32 == 0. */
+tkg_status tkg_quantize_nvfp4(int rows, int k, const float *X, void *Q, void *sf, float *tensor_scale,
+                              cudaStream_t stream);
+
+/* Process-wide tuning and test options (all default to 0 = automatic). */
+typedef enum {
+  TKG_OPT_CTA_GROUP = 1,      /* 0 auto, 1 single-CTA MMA, 2 CTA-pair MMA */
+  TKG_OPT_SINGLE_STAGE = 2,   /* 1: run the one-stage pipeline build (a test of the ring) */
+  TKG_OPT_TIMEOUT_MS = 3,     /* bound on every device wait, milliseconds (0: 1000) */
+  TKG_OPT_INJECT_STALL = 4,   /* 1: the MMA role waits on a barrier nothing arrives on
+                                  (test of the timeout path; output is garbage) */
+  TKG_OPT_MAX_CLUSTERS = 5    /* cap on persistent clusters (0: fill the GPU) */
+} tkg_option;
+
+tkg_status tkg_set_option(tkg_option option, int value);
+int tkg_get_option(tkg_option option);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TKG_GEMM_H */

@@ -1,0 +1,72 @@
+"""The C ABI: the library builds for sm_103a, loads, exports every function that
+include/tkg_gemm.h declares, and rejects bad arguments on the host before any
+CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tkg_gemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tkg_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_block_scaled_gb300 import build, tkg
+    build.build()
+    return tkg.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    from dense_block_scaled_gb300 import tkg
+    assert set(names) == set(tkg.EXPORTS)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_host_side_argument_checks(lib):
+    from dense_block_scaled_gb300 import tkg
+    # negative sizes are rejected before anything touches CUDA
+    assert tkg.gemm_bf16_raw(-1, 8, 8, 16, 16, 16, 1.0, None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_mxfp8_raw(8, -8, 32, 16, 16, 16, 16, 16, 1.0, None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_nvfp4_raw(8, 8, -32, 16, 16, 16, 16, None, None, 16, 1.0, None) == tkg.ERR_INVALID_ARG
+    # empty GEMMs are a no-op
+    assert tkg.gemm_bf16_raw(0, 8, 8, None, None, None, 1.0, None) == tkg.OK
+    assert tkg.gemm_nvfp4_raw(8, 0, 32, None, None, None, None, None, None, None, 1.0, None) == tkg.OK
+    # misaligned output pitch / pointer
+    assert tkg.gemm_bf16_raw(8, 12, 8, 16, 16, 16, 1.0, None) == tkg.ERR_ALIGNMENT
+    assert tkg.gemm_bf16_raw(8, 8, 8, 16, 16, 24, 1.0, None) == tkg.ERR_ALIGNMENT
+    assert tkg.gemm_bf16_raw(8, 8, 8, None, 16, 16, 1.0, None) == tkg.ERR_INVALID_ARG
+
+
+def test_scale_bytes(lib):
+    from dense_block_scaled_gb300 import tkg
+    assert tkg.scale_bytes(1, 32, 32) == 128 * 4
+    assert tkg.scale_bytes(128, 128, 32) == 128 * 4
+    assert tkg.scale_bytes(129, 4000, 16) == 256 * 252
+    assert tkg.scale_bytes(16384, 16384, 16) == 16384 * 1024
+    assert tkg.scale_bytes(5, 64, 8) == 0
+
+
+def test_options_roundtrip(lib):
+    from dense_block_scaled_gb300 import tkg
+    tkg.set_option(tkg.OPT_CTA_GROUP, 2)
+    assert tkg.get_option(tkg.OPT_CTA_GROUP) == 2
+    tkg.set_option(tkg.OPT_CTA_GROUP, 0)
+    with pytest.raises(tkg.TkgError):
+        tkg.set_option(tkg.OPT_CTA_GROUP, 3)
+    assert lib.tkg_status_string(5) == b"device wait timed out"
+
+
+def test_library_is_sm103a_only():
+    # the build passes exactly one -gencode, for sm_103a
+    from dense_block_scaled_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

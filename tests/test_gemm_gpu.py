@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA GEMMs (through the C ABI) against the CPU oracle.
+
+Acceptance bound per element: |D - ref| <= 2^-7 |ref| + 1e-5 * sum_k |alpha a_k b_k|;
+exact equality for the format-decode and scale-index cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_block_scaled_gb300 import tkg
+from helpers import Operands, assert_within_tolerance, bf16_to_f64, run_gemm, tiled_scales, to_dev
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["bf16", "mxfp8", "nvfp4"]
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    for o in (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
+              tkg.OPT_MAX_CLUSTERS):
+        tkg.set_option(o, 0)
+    yield
+    for o in (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
+              tkg.OPT_MAX_CLUSTERS):
+        tkg.set_option(o, 0)
+
+
+def _check(fmt, m, n, k, seed, alpha=1.0, cta_group=0):
+    tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    ops = Operands(fmt, m, n, k, seed, alpha)
+    D = run_gemm(fmt, ops.upload(), m, n, k, alpha)
+    assert tkg.device_status() == tkg.OK
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, f"{fmt} {m}x{n}x{k} cg={cta_group}")
+    return D
+
+
+# 512^3 (the small square workload), several tiles with ragged M/N/K tails
+SHAPES = [(512, 512, 512), (300, 264, 320), (129, 136, 96), (1, 8, 32), (257, 520, 1056)]
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_gemm_matches_oracle(fmt, shape, cta_group):
+    m, n, k = shape
+    _check(fmt, m, n, k, seed=1000 + m + n + k, alpha=1.0, cta_group=cta_group)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_alpha_and_k_tail(fmt):
+    # K = 4000: not a multiple of any stage depth; alpha != 1
+    _check(fmt, 200, 136, 4000, seed=7, alpha=-0.375)
+
+
+def test_bf16_odd_k():
+    _check("bf16", 130, 24, 40, seed=8)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_many_tiles_per_cta(fmt):
+    # few persistent clusters: every CTA walks many tiles, the stage and
+    # accumulator phases wrap many times
+    tkg.set_option(tkg.OPT_MAX_CLUSTERS, 3)
+    _check(fmt, 1024, 1024, 512, seed=9)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_single_stage_equals_deep_pipeline(fmt):
+    # pipeline depth 1 and the deep ring must give identical bits ("异步Tensor Core原理与实战", §5.2)
+    m, n, k = 384, 512, 1024
+    ops = Operands(fmt, m, n, k, seed=11)
+    dev = ops.upload()
+    D_deep = run_gemm(fmt, dev, m, n, k, 1.0)
+    tkg.set_option(tkg.OPT_SINGLE_STAGE, 1)
+    D_one = run_gemm(fmt, dev, m, n, k, 1.0)
+    tkg.set_option(tkg.OPT_SINGLE_STAGE, 0)
+    assert tkg.device_status() == tkg.OK
+    assert torch.equal(D_deep.view(torch.int16), D_one.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_repeatable_bits(fmt):
+    m, n, k = 512, 256, 768
+    ops = Operands(fmt, m, n, k, seed=12)
+    dev = ops.upload()
+    D1 = run_gemm(fmt, dev, m, n, k, 1.0)
+    D2 = run_gemm(fmt, dev, m, n, k, 1.0)
+    assert torch.equal(D1.view(torch.int16), D2.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_guard_bands_untouched(fmt):
+    m, n, k = 200, 136, 256
+    ops = Operands(fmt, m, n, k, seed=13)
+    pad = 4096
+    buf = torch.full((pad + m * n + pad,), 0x5A5A, dtype=torch.int16, device="cuda")
+    D = buf[pad:pad + m * n].view(torch.bfloat16).view(m, n)
+    run_gemm(fmt, ops.upload(), m, n, k, 1.0, D=D)
+    assert tkg.device_status() == tkg.OK
+    host = buf.cpu()
+    assert bool((host[:pad] == 0x5A5A).all()) and bool((host[pad + m * n:] == 0x5A5A).all())
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, "guarded")
+
+
+def test_empty_and_k0():
+    from dense_block_scaled_gb300 import tkg as t
+    D = torch.full((4, 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    A = torch.zeros((4, 8), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((8, 8), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert t.gemm_bf16_raw(0, 8, 8, A.data_ptr(), B.data_ptr(), D.data_ptr(), 1.0, s) == t.OK
+    assert bool((D == 3.0).all())
+    assert t.gemm_bf16_raw(4, 8, 0, A.data_ptr(), B.data_ptr(), D.data_ptr(), 1.0, s) == t.OK
+    torch.cuda.synchronize()
+    assert bool((D == 0).all())
+    assert t.gemm_bf16_raw(4, 8, 12, A.data_ptr(), B.data_ptr(), D.data_ptr(), 1.0, s) == t.ERR_ALIGNMENT
+    assert t.gemm_bf16_raw(4, 8, 8, A.data_ptr() + 2, B.data_ptr(), D.data_ptr(), 1.0, s) == t.ERR_ALIGNMENT
+
+
+# --------------------------------------------------------------------------- exact cases
+
+def test_bf16_every_code_exact():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ex = (codes >> 7) & 0xFF
+    keep = codes[(ex != 0xFF) & ((ex != 0) | ((codes & 0x7F) == 0))]   # no Inf/NaN, no subnormals
+    m = keep.size
+    k, n = 8, 8
+    A = np.zeros((m, k), np.uint16)
+    A[:, 0] = keep
+    B = np.zeros((n, k), np.uint16)
+    B[0, 0] = 0x3F80          # 1.0
+    D = run_gemm("bf16", (to_dev(A), to_dev(B), None, None, None, None), m, n, k, 1.0)
+    ref, _ = oracle.gemm("bf16", A, B)
+    got = bf16_to_f64(D)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_every_code_pair_exact(fmt, cta_group):
+    tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    k = 32
+    if fmt == "mxfp8":
+        codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+        rows = 256
+        A = np.zeros((rows, k), np.uint8)
+        A[:len(codes), 0] = codes
+        unit = 127
+    else:
+        codes = list(range(16))
+        rows = 16
+        A = np.zeros((rows, k // 2), np.uint8)
+        A[:, 0] = codes
+        unit = 0x38
+    B = A.copy()
+    ld = oracle.ld_sf(k, fmt)
+    sf = np.full((rows, ld), unit, np.uint8)
+    kb = k // oracle.BLOCK[fmt]
+    dev = (to_dev(A), to_dev(B), to_dev(tiled_scales(sf, kb)), to_dev(tiled_scales(sf, kb)), None, None)
+    D = run_gemm(fmt, dev, rows, rows, k, 1.0)
+    ref, _ = oracle.gemm(fmt, A, B, sf, sf, 1.0)
+    assert np.array_equal(bf16_to_f64(D), ref)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_scale_index_exact(fmt, cta_group):
+    # one nonzero block per row; distinct scale codes per (row, block); rows
+    # cross 128-row tiles and the CTA pair, blocks cross stages and atoms
+    tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    bs = oracle.BLOCK[fmt]
+    m, n, k = 520, 264, 1536
+    kb = k // bs
+    rng = np.random.default_rng(31)
+    lo, hi = (110, 145) if fmt == "mxfp8" else (0x28, 0x50)
+    ld = oracle.ld_sf(k, fmt)
+    sfa = rng.integers(lo, hi, size=(m, ld)).astype(np.uint8)
+    sfb = rng.integers(lo, hi, size=(n, ld)).astype(np.uint8)
+    blk_a = rng.integers(0, kb, size=m)
+    blk_b = blk_a[rng.integers(0, m, size=n)]      # many (i, j) share a block
+    one = 0x38 if fmt == "mxfp8" else 0x2
+
+    def fill(rows, blk):
+        if fmt == "mxfp8":
+            X = np.zeros((rows, k), np.uint8)
+            for r in range(rows):
+                X[r, blk[r] * bs] = one
+        else:
+            X = np.zeros((rows, k // 2), np.uint8)
+            for r in range(rows):
+                X[r, blk[r] * bs // 2] = one
+        return X
+
+    A, B = fill(m, blk_a), fill(n, blk_b)
+    dev = (to_dev(A), to_dev(B), to_dev(tiled_scales(sfa, kb)), to_dev(tiled_scales(sfb, kb)), None, None)
+    D = run_gemm(fmt, dev, m, n, k, 1.0)
+    ref, _ = oracle.gemm(fmt, A, B, sfa, sfb, 1.0)
+    assert np.count_nonzero(ref) > 1000
+    assert np.array_equal(bf16_to_f64(D), ref)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_every_scale_code_against_unit(fmt):
+    # each scale code on A's side times a unit scale on B's side
+    if fmt == "mxfp8":
+        codes, unit, k = list(range(1, 255)), 127, 32
+    else:
+        codes, unit, k = list(range(0x01, 0x7F)), 0x38, 32
+    m = 256
+    bs = oracle.BLOCK[fmt]
+    ld = oracle.ld_sf(k, fmt)
+    sfa = np.full((m, ld), unit, np.uint8)
+    sfa[:len(codes), 0] = codes
+    sfb = np.full((8, ld), unit, np.uint8)
+    if fmt == "mxfp8":
+        A = np.zeros((m, k), np.uint8)
+        A[:, 0] = 0x38
+        B = np.zeros((8, k), np.uint8)
+        B[0, 0] = 0x38
+    else:
+        A = np.zeros((m, k // 2), np.uint8)
+        A[:, 0] = 0x2
+        B = np.zeros((8, k // 2), np.uint8)
+        B[0, 0] = 0x2
+    kb = k // bs
+    dev = (to_dev(A), to_dev(B), to_dev(tiled_scales(sfa, kb)), to_dev(tiled_scales(sfb, kb)), None, None)
+    D = run_gemm(fmt, dev, m, 8, k, 1.0)
+    ref, _ = oracle.gemm(fmt, A, B, sfa, sfb, 1.0)
+    assert np.array_equal(bf16_to_f64(D), ref)
+
+
+# --------------------------------------------------------------------------- full size, sampled
+
+FULL = [("bf16", 16384), ("mxfp8", 16384), ("nvfp4", 16384), ("bf16", 4000), ("nvfp4", 4000)]
+
+
+@pytest.mark.parametrize("fmt,size", FULL)
+def test_full_size_sampled(fmt, size):
+    m = n = k = size
+    ops = Operands(fmt, m, n, k, seed=1000 + size)
+    dev = ops.upload()
+    D = run_gemm(fmt, dev, m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    rng = np.random.default_rng(size)
+    ii = np.concatenate([rng.integers(0, m, 3000), [0, m - 1, m - 1, 0, 255, 256, 127, 128]])
+    jj = np.concatenate([rng.integers(0, n, 3000), [0, n - 1, 0, n - 1, 256, 255, 128, 127]])
+    ref, S = ops.reference_elems(ii, jj)
+    got = bf16_to_f64(D[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()])
+    assert_within_tolerance(got, ref, S, f"{fmt} {size}^3 sampled")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("m", [16, 128, 1024])
+def test_skinny_full_size(fmt, m):
+    n = k = 8192
+    ops = Operands(fmt, m, n, k, seed=1004)
+    D = run_gemm(fmt, ops.upload(), m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    rows = min(m, 16)
+    ref, S = ops.reference(rows=(m - rows, rows))
+    assert_within_tolerance(bf16_to_f64(D[m - rows:]), ref, S, f"{fmt} skinny m={m}")
