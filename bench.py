@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""GEMM throughput on one GB300 (or N, as independent replicas), following the
+benchmark method of "ThunderKittens 2.0 GPU Kernel优化" §五: bit-identical
+seeded inputs, W warm-up launches, K timed back-to-back launches between two
+CUDA events, input groups rotated so that every launch reads cold L2
+(groups = 1 if the inputs are >= 3x L2, else floor(3 L2 / size) + 1), clocks
+sampled during the run.
+
+Headline: BF16 D = A.B^T at M=N=K=16384 (the largest point of the BF16 square
+sweep), TFLOP/s = 2MNK / t.  The same JSON line carries the rest of the BF16
+sweep and the MXFP8 / NVFP4 16384^3 GEMMs (operands quantised on the GPU by the
+library's own quantisers), each with its roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain FP64 reference GEMM) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PAGES_PEAK_TFLOPS = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 9000.0}   # HGX B200 dense figures the pages list
+NOMINAL_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}                 # GB300 dense fp8/fp4 vs bf16 (4.5, 13.5 vs 2.25 PF)
+SEEDS = {"bf16": 1001, "mxfp8": 1002, "nvfp4": 1003}                      # 1000 + workload index
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--size", type=int, default=16384, help="headline M=N=K")
+    ap.add_argument("--formats", default="bf16,mxfp8,nvfp4")
+    ap.add_argument("--sweep", default="2048,4096,8192", help="extra BF16 sizes reported beside the headline")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-rows", type=int, default=48, help="rows of the oracle's CPU-baseline sample")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- environment
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16": float(d["bf16_tflops"]), "bf16_sustained": float(d.get("bf16_tflops_sustained", 0) or 0),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("ptx.cuh", "gemm_kernel.cuh", "host_common.cuh", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_nvfp4.cu"):
+        h.update(open(os.path.join(ROOT, "dense_block_scaled_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch recorded from an ncu capture, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.uuid = device_uuid
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(prefix="clk", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.out.name):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), f[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Workload:
+    """One GEMM (format, M=N=K=size) resident in HBM in `groups` identical copies."""
+
+    def __init__(self, fmt, size, seed, l2_bytes, torch, tkg, synth, keep_host=False):
+        self.fmt, self.size = fmt, size
+        self.m = self.n = self.k = size
+        t0 = time.time()
+        a, b = synth.gemm_inputs_f32(size, size, size, seed)
+        dev = torch.device("cuda")
+        self.host = None
+        if fmt == "bf16":
+            ca, cb = synth.bf16_codes(a), synth.bf16_codes(b)
+            del a, b
+            A = torch.from_numpy(ca.view("int16")).view(torch.bfloat16)
+            B = torch.from_numpy(cb.view("int16")).view(torch.bfloat16)
+            ops = [A.to(dev), B.to(dev), None, None, None, None]
+            if keep_host:
+                self.host = (ca, cb)
+        else:
+            X = torch.from_numpy(a).to(dev)
+            Y = torch.from_numpy(b).to(dev)
+            del a, b
+            bs = 32 if fmt == "mxfp8" else 16
+            cols = size if fmt == "mxfp8" else size // 2
+            QA = torch.empty((size, cols), dtype=torch.uint8, device=dev)
+            QB = torch.empty((size, cols), dtype=torch.uint8, device=dev)
+            SA = torch.empty((tkg.scale_bytes(size, size, bs),), dtype=torch.uint8, device=dev)
+            SB = torch.empty((tkg.scale_bytes(size, size, bs),), dtype=torch.uint8, device=dev)
+            if fmt == "mxfp8":
+                tkg.quantize_mxfp8(X, QA, SA)
+                tkg.quantize_mxfp8(Y, QB, SB)
+                ops = [QA, QB, SA, SB, None, None]
+            else:
+                TA = torch.empty(1, dtype=torch.float32, device=dev)
+                TB = torch.empty(1, dtype=torch.float32, device=dev)
+                tkg.quantize_nvfp4(X, QA, SA, TA)
+                tkg.quantize_nvfp4(Y, QB, SB, TB)
+                ops = [QA, QB, SA, SB, TA, TB]
+            del X, Y
+            torch.cuda.synchronize()
+        self.in_bytes = sum(int(o.numel() * o.element_size()) for o in ops if o is not None)
+        self.out_bytes = self.m * self.n * 2
+        self.groups = 1 if self.in_bytes >= 3 * l2_bytes else (3 * l2_bytes) // self.in_bytes + 1
+        self.sets = [ops] + [[o.clone() if o is not None else None for o in ops] for _ in range(self.groups - 1)]
+        self.D = [torch.empty((self.m, self.n), dtype=torch.bfloat16, device=dev) for _ in range(self.groups)]
+        self.flop = 2.0 * self.m * self.n * self.k
+        self.prep_s = time.time() - t0
+
+    def launch(self, i, tkg):
+        A, B, sa, sb, ta, tb = self.sets[i % self.groups]
+        D = self.D[i % self.groups]
+        if self.fmt == "bf16":
+            tkg.gemm_bf16(A, B, D, 1.0)
+        elif self.fmt == "mxfp8":
+            tkg.gemm_mxfp8(A, B, sa, sb, D, 1.0)
+        else:
+            tkg.gemm_nvfp4(A, B, sa, sb, D, 1.0, ta=ta, tb=tb)
+
+
+def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flush_buf=None):
+    """Seconds per launch: W untimed launches, then K timed back to back between
+    two events on the launching stream (or one event pair per launch around an
+    explicit L2 flush when l2_mode == 'flush')."""
+    for i in range(warmup):
+        w.launch(i, tkg)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if l2_mode == "flush":
+        total = 0.0
+        for i in range(steps):
+            flush_buf.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            w.launch(i, tkg)
+            e1.record()
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+        ms = total
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            w.launch(i, tkg)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    st = tkg.device_status()
+    if st != tkg.OK:
+        raise RuntimeError(f"device status after timing: {tkg.status_string(st)}")
+    return ms / 1e3 / steps
+
+
+def e2e_seconds(w, steps, torch, tkg):
+    """Per-step seconds through the public API with HOST buffers: pinned inputs
+    copied to the device, the GEMM, the output copied back, all timed."""
+    A, B, sa, sb, ta, tb = w.sets[0]
+    dev_ops = [A, B, sa, sb, ta, tb]
+    host = [o.cpu().pin_memory() if o is not None else None for o in dev_ops]
+    Dh = torch.empty((w.m, w.n), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(int(h.numel() * h.element_size()) for h in host if h is not None)
+    d2h = int(Dh.numel() * Dh.element_size())
+
+    def step():
+        for h, d in zip(host, dev_ops):
+            if h is not None:
+                d.copy_(h, non_blocking=True)
+        w.launch(0, tkg)
+        Dh.copy_(w.D[0], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+
+
+def cpu_baseline(A, B, size, rows):
+    """The oracle, as it stands, on a band of `rows` rows of the headline workload
+    (A, B: its host BF16 codes)."""
+    import oracle
+    oracle.build()
+    t0 = time.time()
+    oracle.gemm("bf16", A[:rows], B)
+    dt = time.time() - t0
+    return {"value": 2.0 * rows * size * size / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"rows 0..{rows - 1} of A against all {size} rows of B, K={size} "
+                                        f"(FP64, {dt:.1f} s)"}
+
+
+# --------------------------------------------------------------------------- arms
+
+def headline_config(size, l2_desc):
+    return {"workload": f"BF16 GEMM M=N=K={size}", "A": f"{size}x{size} bf16 N(0,1) seed {SEEDS['bf16']}",
+            "B": f"{size}x{size} bf16 N(0,1)", "alpha": 1.0, "accumulate": "fp32", "output": "bf16",
+            "l2": l2_desc}
+
+
+def l2_description(groups, mode):
+    if mode == "flush":
+        return "explicit flush (2x L2 write) before every launch"
+    return "inputs larger than 3x L2, no rotation needed" if groups == 1 else f"{groups} rotated input groups"
+
+
+def run_reference(args):
+    """CPU oracle on the host cores: each step = a sample of output elements."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from dense_block_scaled_gb300 import synth
+    size = args.size
+    oracle.build()
+    a_rows = 64
+    a, b = synth.gemm_inputs_f32(size, size, size, SEEDS["bf16"])   # the whole workload, as the GPU arm
+    A, B = synth.bf16_codes(a[:a_rows]), synth.bf16_codes(b)
+    del a, b
+    rng = np.random.default_rng(0)
+    per_step = 256
+    ii = rng.integers(0, a_rows, size=(args.warmup + args.steps, per_step))
+    jj = rng.integers(0, size, size=(args.warmup + args.steps, per_step))
+    for s in range(args.warmup):
+        oracle.gemm_elems("bf16", A, B, None, None, 1.0, ii[s], jj[s])
+    t0 = time.time()
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.gemm_elems("bf16", A, B, None, None, 1.0, ii[s], jj[s])
+    dt = (time.time() - t0) / max(args.steps, 1)
+    value = 2.0 * per_step * size / dt / 1e12
+    line = {
+        "impl": "reference", "metric": "GEMM TFLOP/s (BF16 D=A.B^T, M=N=K=%d)" % size, "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": dict(headline_config(size, l2_description(1 if size >= 8192 else 2, "rotate")),
+                       sample_per_step=f"{per_step} output elements"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} random output elements per step, each a K={size} FP64 dot product"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from dense_block_scaled_gb300 import build, synth, tkg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    tkg.load()
+    pk = peaks()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
+
+    formats = [f for f in args.formats.split(",") if f]
+    head = Workload("bf16", args.size, SEEDS["bf16"], l2, torch, tkg, synth, keep_host=(rank == 0 and not args.no_cpu))
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda") if args.l2 == "flush" else None
+
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    t_head = time_launches(head, args.steps, args.warmup, torch, tkg, dist, args.l2, flush_buf)
+    clk = clocks.stop()
+
+    # max over ranks
+    t_max = t_head
+    if dist is not None:
+        tt = torch.tensor([t_head], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = world * head.flop / t_max / 1e12
+    achieved = head.flop / t_head / 1e12
+
+    by_format = {}
+    sweep = {}
+    e2e = None
+    if rank == 0:
+        for fmt in formats:
+            if fmt == "bf16":
+                w, t = head, t_head
+            else:
+                w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth)
+                t = time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2, flush_buf)
+            tf = w.flop / t / 1e12
+            peak_meas = pk["bf16"] * NOMINAL_RATIO[fmt]
+            by_format[fmt] = {"tflops": tf, "ms": t * 1e3, "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[fmt],
+                              "pages_peak_tflops": PAGES_PEAK_TFLOPS[fmt], "frac_of_measured": tf / peak_meas,
+                              "measured_peak_tflops": peak_meas, "input_groups": w.groups}
+            if w is not head:
+                del w
+                torch.cuda.empty_cache()
+        for s in [int(x) for x in args.sweep.split(",") if x]:
+            w = Workload("bf16", s, SEEDS["bf16"], l2, torch, tkg, synth)
+            t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+            sweep[str(s)] = {"tflops": w.flop / t / 1e12, "us": t * 1e6, "input_groups": w.groups,
+                             "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS["bf16"]}
+            del w
+            torch.cuda.empty_cache()
+        if not args.no_e2e:
+            te, h2d, d2h = e2e_seconds(head, args.e2e_steps, torch, tkg)
+            e2e = {"value": world * head.flop / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(head.host[0], head.host[1], args.size, args.cpu_rows)
+
+    if rank == 0:
+        workload = f"BF16 GEMM M=N=K={args.size}"
+        peak = pk["bf16"]
+        line = {
+            "metric": f"GEMM TFLOP/s (BF16 D=A.B^T, M=N=K={args.size})",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_max * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": dict(headline_config(args.size, l2_description(head.groups, args.l2)),
+                           frac_of_pages_peak=value / world / PAGES_PEAK_TFLOPS["bf16"],
+                           pages_peak_tflops=PAGES_PEAK_TFLOPS["bf16"], replicas=world),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(workload),
+                         "peak_source": f"{pk['source']} cuBLAS bf16 burst",
+                         "frac_of_sustained": achieved / pk["bf16_sustained"] if pk["bf16_sustained"] else None},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clk,
+            "formats": by_format,
+            "sweep_bf16": sweep,
+            "kernel_hash": kernel_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -32,7 +32,7 @@ def gemm_inputs_f32(m: int, n: int, k: int, seed: int):
 def bf16_codes(x: np.ndarray) -> np.ndarray:
     """uint16 bit patterns of x cast to bfloat16 (torch's round-to-nearest-even cast)."""
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
-    return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.view(torch.int16).numpy().view(np.uint16)
 
 
 def random_codes(shape, n_codes: int, seed: int, exclude=()) -> np.ndarray:

@@ -1,0 +1,41 @@
+"""Bounded waits: a GEMM whose MMA role waits on a barrier that nothing ever
+arrives on must return within the wait limit, report TKG_ERR_TIMEOUT through
+tkg_get_device_status, and leave the context usable for the next GEMM.
+No fault, trap or hang is involved: the kernel gives up on its own."""
+import time
+
+import pytest
+import torch
+
+from dense_block_scaled_gb300 import tkg
+from helpers import Operands, assert_within_tolerance, bf16_to_f64, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_stalled_wait_times_out_and_recovers(fmt, cta_group):
+    m, n, k = 512, 512, 1024
+    ops = Operands(fmt, m, n, k, seed=77)
+    dev = ops.upload()
+    tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    try:
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 100)
+        tkg.set_option(tkg.OPT_INJECT_STALL, 1)
+        t0 = time.time()
+        run_gemm(fmt, dev, m, n, k, 1.0)
+        st = tkg.device_status()
+        elapsed = time.time() - t0
+        assert st == tkg.ERR_TIMEOUT
+        assert elapsed < 10.0
+    finally:
+        tkg.set_option(tkg.OPT_INJECT_STALL, 0)
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 0)
+    # the status word was cleared and the next launch is healthy
+    D = run_gemm(fmt, dev, m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, "after recovery")
+    tkg.set_option(tkg.OPT_CTA_GROUP, 0)
+    torch.cuda.synchronize()
