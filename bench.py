@@ -46,7 +46,10 @@ def parse_args():
     ap.add_argument("--formats", default="bf16,mxfp8,nvfp4")
     ap.add_argument("--sweep", default="2048,4096,8192", help="extra BF16 sizes reported beside the headline")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-rows", type=int, default=48, help="rows of the oracle's CPU-baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=768, help="rows of the oracle's CPU-baseline sample")
+    ap.add_argument("--head-format", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
+                    help="format of the first (timed, clock-sampled) workload; profiling runs pick it")
+    ap.add_argument("--skinny", default="16,128,1024", help="M values of the skinny N=K=8192 GEMMs reported")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
@@ -135,11 +138,12 @@ class ClockSampler:
 class Workload:
     """One GEMM (format, M=N=K=size) resident in HBM in `groups` identical copies."""
 
-    def __init__(self, fmt, size, seed, l2_bytes, torch, tkg, synth, keep_host=False):
+    def __init__(self, fmt, size, seed, l2_bytes, torch, tkg, synth, keep_host=False, mnk=None):
         self.fmt, self.size = fmt, size
-        self.m = self.n = self.k = size
+        self.m, self.n, self.k = mnk if mnk else (size, size, size)
+        m, n, k = self.m, self.n, self.k
         t0 = time.time()
-        a, b = synth.gemm_inputs_f32(size, size, size, seed)
+        a, b = synth.gemm_inputs_f32(m, n, k, seed)
         dev = torch.device("cuda")
         self.host = None
         if fmt == "bf16":
@@ -155,11 +159,11 @@ class Workload:
             Y = torch.from_numpy(b).to(dev)
             del a, b
             bs = 32 if fmt == "mxfp8" else 16
-            cols = size if fmt == "mxfp8" else size // 2
-            QA = torch.empty((size, cols), dtype=torch.uint8, device=dev)
-            QB = torch.empty((size, cols), dtype=torch.uint8, device=dev)
-            SA = torch.empty((tkg.scale_bytes(size, size, bs),), dtype=torch.uint8, device=dev)
-            SB = torch.empty((tkg.scale_bytes(size, size, bs),), dtype=torch.uint8, device=dev)
+            cols = k if fmt == "mxfp8" else k // 2
+            QA = torch.empty((m, cols), dtype=torch.uint8, device=dev)
+            QB = torch.empty((n, cols), dtype=torch.uint8, device=dev)
+            SA = torch.empty((tkg.scale_bytes(m, k, bs),), dtype=torch.uint8, device=dev)
+            SB = torch.empty((tkg.scale_bytes(n, k, bs),), dtype=torch.uint8, device=dev)
             if fmt == "mxfp8":
                 tkg.quantize_mxfp8(X, QA, SA)
                 tkg.quantize_mxfp8(Y, QB, SB)
@@ -349,7 +353,9 @@ def run_ours(args):
     uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
 
     formats = [f for f in args.formats.split(",") if f]
-    head = Workload("bf16", args.size, SEEDS["bf16"], l2, torch, tkg, synth, keep_host=(rank == 0 and not args.no_cpu))
+    hf = args.head_format
+    head = Workload(hf, args.size, SEEDS[hf], l2, torch, tkg, synth,
+                    keep_host=(rank == 0 and not args.no_cpu and hf == "bf16"))
     flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda") if args.l2 == "flush" else None
 
     clocks = ClockSampler(uuid)
@@ -366,24 +372,25 @@ def run_ours(args):
     value = world * head.flop / t_max / 1e12
     achieved = head.flop / t_head / 1e12
 
-    by_format = {}
-    sweep = {}
+    def fmt_entry(w, t):
+        tf = w.flop / t / 1e12
+        peak_meas = pk["bf16"] * NOMINAL_RATIO[w.fmt]
+        return {"tflops": tf, "ms": t * 1e3, "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[w.fmt],
+                "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
+                "measured_peak_tflops": peak_meas, "input_groups": w.groups}
+
+    by_format, sweep, skinny = {}, {}, {}
     e2e = None
     if rank == 0:
+        by_format[hf] = fmt_entry(head, t_head)
         for fmt in formats:
-            if fmt == "bf16":
-                w, t = head, t_head
-            else:
-                w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth)
-                t = time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2, flush_buf)
-            tf = w.flop / t / 1e12
-            peak_meas = pk["bf16"] * NOMINAL_RATIO[fmt]
-            by_format[fmt] = {"tflops": tf, "ms": t * 1e3, "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[fmt],
-                              "pages_peak_tflops": PAGES_PEAK_TFLOPS[fmt], "frac_of_measured": tf / peak_meas,
-                              "measured_peak_tflops": peak_meas, "input_groups": w.groups}
-            if w is not head:
-                del w
-                torch.cuda.empty_cache()
+            if fmt == hf:
+                continue
+            w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth)
+            by_format[fmt] = fmt_entry(w, time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2,
+                                                          flush_buf))
+            del w
+            torch.cuda.empty_cache()
         for s in [int(x) for x in args.sweep.split(",") if x]:
             w = Workload("bf16", s, SEEDS["bf16"], l2, torch, tkg, synth)
             t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
@@ -391,36 +398,52 @@ def run_ours(args):
                              "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS["bf16"]}
             del w
             torch.cuda.empty_cache()
+        for fmt in ("bf16", "nvfp4"):
+            for mm in [int(x) for x in args.skinny.split(",") if x]:
+                w = Workload(fmt, 8192, 1004, l2, torch, tkg, synth, mnk=(mm, 8192, 8192))
+                t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+                byts = w.in_bytes + w.out_bytes
+                tf = w.flop / t / 1e12
+                roof = min(PAGES_PEAK_TFLOPS[fmt], w.flop / byts * pk["hbm_gbs"] / 1e3)
+                skinny[f"{fmt} M={mm} N=K=8192"] = {
+                    "us": t * 1e6, "tflops": tf, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / pk["hbm_gbs"],
+                    "roofline_tflops": roof, "frac_of_roofline": tf / roof, "input_groups": w.groups}
+                del w
+                torch.cuda.empty_cache()
         if not args.no_e2e:
             te, h2d, d2h = e2e_seconds(head, args.e2e_steps, torch, tkg)
             e2e = {"value": world * head.flop / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
 
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and not args.no_cpu and head.host is not None:
         cpu = cpu_baseline(head.host[0], head.host[1], args.size, args.cpu_rows)
 
     if rank == 0:
-        workload = f"BF16 GEMM M=N=K={args.size}"
-        peak = pk["bf16"]
+        name = {"bf16": "BF16", "mxfp8": "MXFP8", "nvfp4": "NVFP4"}[hf]
+        workload = f"{name} GEMM M=N=K={args.size}"
+        peak = pk["bf16"] * NOMINAL_RATIO[hf]
         line = {
-            "metric": f"GEMM TFLOP/s (BF16 D=A.B^T, M=N=K={args.size})",
+            "metric": f"GEMM TFLOP/s ({name} D=A.B^T, M=N=K={args.size})",
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_max * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": dict(headline_config(args.size, l2_description(head.groups, args.l2)),
-                           frac_of_pages_peak=value / world / PAGES_PEAK_TFLOPS["bf16"],
-                           pages_peak_tflops=PAGES_PEAK_TFLOPS["bf16"], replicas=world),
+            "dtype": hf, "data": "synthetic",
+            "config": dict(headline_config(args.size, l2_description(head.groups, args.l2)) if hf == "bf16"
+                           else {"workload": workload, "l2": l2_description(head.groups, args.l2)},
+                           frac_of_pages_peak=value / world / PAGES_PEAK_TFLOPS[hf],
+                           pages_peak_tflops=PAGES_PEAK_TFLOPS[hf], replicas=world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(workload),
-                         "peak_source": f"{pk['source']} cuBLAS bf16 burst",
-                         "frac_of_sustained": achieved / pk["bf16_sustained"] if pk["bf16_sustained"] else None},
+                         "peak_source": f"{pk['source']} cuBLAS bf16 burst x {NOMINAL_RATIO[hf]:g} (nominal {hf}/bf16)",
+                         "frac_of_sustained": (achieved / (pk["bf16_sustained"] * NOMINAL_RATIO[hf])
+                                               if pk["bf16_sustained"] else None)},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clk,
             "formats": by_format,
             "sweep_bf16": sweep,
+            "skinny": skinny,
             "kernel_hash": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

@@ -131,7 +131,8 @@ typedef enum {
   TKG_OPT_TIMEOUT_MS = 3,     /* bound on every device wait, milliseconds (0: 1000) */
   TKG_OPT_INJECT_STALL = 4,   /* 1: the MMA role waits on a barrier nothing arrives on
                                   (test of the timeout path; output is garbage) */
-  TKG_OPT_MAX_CLUSTERS = 5    /* cap on persistent clusters (0: fill the GPU) */
+  TKG_OPT_MAX_CLUSTERS = 5,   /* cap on persistent clusters (0: fill the GPU) */
+  TKG_OPT_ACC_STAGES = 6      /* BF16 only: 1 = single accumulator buffer (0: double) */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);
