@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtkg.so")
-SOURCES = ["tkg_api.cu", "quantize.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_nvfp4.cu"]
+SOURCES = ["tkg_api.cu", "quantize.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_nvfp4.cu", "gemm_noalloc.cu"]
 HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "host_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

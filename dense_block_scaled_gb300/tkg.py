@@ -23,7 +23,7 @@ OPT_CTA_GROUP, OPT_SINGLE_STAGE, OPT_TIMEOUT_MS, OPT_INJECT_STALL, OPT_MAX_CLUST
 EXPORTS = [
     "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",
     "tkg_scale_bytes", "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
-    "tkg_set_option", "tkg_get_option",
+    "tkg_set_option", "tkg_get_option", "tkg_gemm_bf16_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -46,6 +46,7 @@ def load() -> ctypes.CDLL:
             lib = ctypes.CDLL(LIB_PATH)
             i, vp, f, st = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
             lib.tkg_gemm_bf16.argtypes = [i, i, i, vp, vp, vp, f, vp]
+            lib.tkg_gemm_bf16_noalloc.argtypes = [i, i, i, vp, vp, vp, f, vp]
             lib.tkg_gemm_mxfp8.argtypes = [i, i, i, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_gemm_nvfp4.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_get_device_status.argtypes = [vp]
@@ -58,7 +59,7 @@ def load() -> ctypes.CDLL:
             lib.tkg_quantize_nvfp4.argtypes = [i, i, vp, vp, vp, vp, vp]
             lib.tkg_set_option.argtypes = [i, i]
             lib.tkg_get_option.argtypes = [i]
-            for name in ("tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status",
+            for name in ("tkg_gemm_bf16", "tkg_gemm_bf16_noalloc", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status",
                          "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4", "tkg_set_option",
                          "tkg_get_option"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -98,6 +99,10 @@ def gemm_bf16_raw(m, n, k, A, B, D, alpha, stream) -> int:
     return load().tkg_gemm_bf16(m, n, k, A, B, D, ctypes.c_float(alpha), stream)
 
 
+def gemm_bf16_noalloc_raw(m, n, k, A, B, D, alpha, stream) -> int:
+    return load().tkg_gemm_bf16_noalloc(m, n, k, A, B, D, ctypes.c_float(alpha), stream)
+
+
 def gemm_mxfp8_raw(m, n, k, A, B, sfa, sfb, D, alpha, stream) -> int:
     return load().tkg_gemm_mxfp8(m, n, k, A, B, sfa, sfb, D, ctypes.c_float(alpha), stream)
 
@@ -113,6 +118,14 @@ def gemm_bf16(A, B, D, alpha: float = 1.0, stream=None) -> None:
     m, k = A.shape
     n = B.shape[0]
     _check(gemm_bf16_raw(m, n, k, _ptr(A), _ptr(B), _ptr(D), alpha, _stream(stream)), "tkg_gemm_bf16")
+
+
+def gemm_bf16_noalloc(A, B, D, alpha: float = 1.0, stream=None) -> None:
+    """As gemm_bf16, through the entry point that allocates no device memory."""
+    m, k = A.shape
+    n = B.shape[0]
+    _check(gemm_bf16_noalloc_raw(m, n, k, _ptr(A), _ptr(B), _ptr(D), alpha, _stream(stream)),
+           "tkg_gemm_bf16_noalloc")
 
 
 def gemm_mxfp8(A, B, sfa, sfb, D, alpha: float = 1.0, stream=None) -> None:

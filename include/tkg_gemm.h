@@ -87,6 +87,30 @@ tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void *A, const void *B, con
                           const float *tensor_scale_a, const float *tensor_scale_b, void *D, float alpha,
                           cudaStream_t stream);
 
+/* BF16 GEMM that allocates nothing, for callers that cannot call cudaMalloc:
+ * runtimes that reserve all of their device memory at start-up and forbid
+ * allocation afterwards, or that run under a memory budget where an
+ * allocation hidden inside a library call must not happen.  (No counterpart
+ * on the pages: this is a property of the library, not of the method.)
+ *
+ * Same arguments, layouts, checks and result as tkg_gemm_bf16, and the same
+ * kernel.  Its scratch -- the status word the kernel sets when a bounded wait
+ * runs out -- lives in a fixed 256-byte array that is part of the library
+ * image (each GPU that loads the library keeps it until the process exits)
+ * instead of memory obtained with cudaMalloc.  The kernel needs 4 bytes of it
+ * whatever m, n and k are; a call whose scratch need exceeded the array would
+ * return TKG_ERR_UNSUPPORTED.
+ *  - The first call on a device does one-time set-up there (it looks up the
+ *    array's device address and sets the kernel's shared-memory limit); make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array and clears the status word
+ *    when it starts, so calls that overlap on the GPU race on it: order them
+ *    on one stream or with events.
+ *  - A timed-out wait in this variant is recorded only in that array, not in
+ *    the word tkg_get_device_status reads; D is then unspecified. */
+tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void *A, const void *B, void *D, float alpha,
+                                 cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: TKG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
  * call (its output is then unspecified), TKG_ERR_CUDA on a CUDA error,
