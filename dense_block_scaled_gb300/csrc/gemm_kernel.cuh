@@ -122,25 +122,34 @@ struct GemmConfig {
   static constexpr int kABytes = kCtaM * kRowBytes;
   static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kSfaBytes = T::kSfAtoms * 512;
-  static constexpr int kSfbBytes = (BN / 128) * T::kSfAtoms * 512;
+  // B scales come in 128-row blocks of the tiled layout; every CTA holds the
+  // whole N tile's scales (the MMA's B scales live in each CTA's tensor memory)
+  static constexpr int kSfbBlocks = BN / 128;
+  static constexpr int kSfbBytes = kScaled ? kSfbBlocks * T::kSfAtoms * 512 : 0;
   static constexpr int kStageBytes = ((kABytes + kBBytes + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
   static constexpr int kMmasPerStage = T::kStageK / T::kMmaK;
   static constexpr int kEpiBufBytes = 32 * 64;      // 32 rows x 32 BF16
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-  static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 * ACC + 2;
-  static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + alignment slack
+  static constexpr int kFixedBytes = kNumBars * 8 + kEpiWarps * 16 + 16 + 1024;   // barriers, signal slots, slack
+  // two staging buffers per epilogue warp when they fit, else one
+  static constexpr int kEpiBufs =
+      STAGES * kStageBytes + kEpiWarps * 2 * kEpiBufBytes + kFixedBytes <= 232448 ? 2 : 1;
+  static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
+  static constexpr int kSmemBytes = kBarOffset + kFixedBytes;
   // bytes landing on the leader's full barrier per stage (all CTAs of the pair)
   static constexpr uint32_t kTxBytes = uint32_t(CG * (kABytes + kBBytes + kSfaBytes + kSfbBytes));
-  // tensor memory
+  // tensor memory: ACC accumulators of BN columns, then a ring of scale
+  // regions (4 columns of A scales + 4 per 128-row block of B scales), one
+  // region per stage (MXFP8) or per MMA (NVFP4)
   static constexpr int kAccCols = BN;
-  static constexpr int kSfaCols = T::kSfAtoms * 4;
-  static constexpr int kSfbCols = (BN / 128) * T::kSfAtoms * 4;
-  static constexpr int kSlotCols = kSfaCols + kSfbCols;
   static constexpr int kScaleBase = ACC * kAccCols;
+  static constexpr int kRegionCols = 4 + 4 * kSfbBlocks;
+  static constexpr int kRegions = kScaled ? (512 - kScaleBase) / kRegionCols : 0;
   static constexpr int kTmemCols = 512;
-  static_assert(ACC * kAccCols + STAGES * kSlotCols <= kTmemCols, "tensor memory overflow");
-  static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
+  static_assert(!kScaled || kRegions >= 2, "tensor memory overflow");
+  static_assert(ACC * kAccCols <= kTmemCols, "tensor memory overflow");
+  static_assert(BN == 128 || BN == 256, "B tiles must cover whole 128-row scale blocks");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static constexpr uint32_t kIdescBase =
       FMT == FMT_BF16 ? idesc_f16(kMmaM, BN)
@@ -190,6 +199,7 @@ __global__ void __launch_bounds__(384, 1)
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC>;
+  using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -202,10 +212,10 @@ __global__ void __launch_bounds__(384, 1)
   // 1024-byte aligned carve-up (identical in both CTAs of a pair)
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* const gbase = smem_raw + (base - raw);
   auto stage_a = [&](int s) { return base + uint32_t(s * C::kStageBytes); };
   auto stage_b = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes); };
   auto stage_sfa = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes); };
+  // B scales: block a (of the loaded ones), atom g at stage_sfb + (a * kSfAtoms + g) * 512
   auto stage_sfb = [&](int s) {
     return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes + C::kSfaBytes);
   };
@@ -217,7 +227,8 @@ __global__ void __launch_bounds__(384, 1)
   auto acce_bar = [&](int a) { return bars + uint32_t(8 * (2 * STAGES + ACC + a)); };
   const uint32_t drain_bar = bars + uint32_t(8 * (2 * STAGES + 2 * ACC));
   const uint32_t never_bar = drain_bar + 8;
-  (void)gbase;
+  // 16-byte landing slots for the follower's "accumulator free" signals (epilogue)
+  auto epi_sig_slot = [&](int w) { return ((never_bar + 8u + 15u) & ~15u) + uint32_t(16 * w); };
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -227,7 +238,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       ptx::mbar_init(accf_bar(a), 1);
-      ptx::mbar_init(acce_bar(a), C::kEpiWarps * CG);
+      ptx::mbar_init(acce_bar(a), C::kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
     ptx::mbar_init(never_bar, 1);
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(384, 1)
     if (ptx::elect_one()) {
       const uint64_t pol_a = ptx::policy_evict_last();
       const uint64_t pol_b = ptx::policy_evict_normal();
-      // barrier the loads complete on: the pair leader's full barrier
+      // barrier the operand loads complete on: the pair leader's full barrier
       const uint32_t lead_full0 = (CG == 2) ? ptx::map_to_rank(full_bar(0), 0) : full_bar(0);
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0;          // stages whose last arming is not yet known complete
@@ -277,6 +288,7 @@ __global__ void __launch_bounds__(384, 1)
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         const int a_row = mb * C::kMmaM + int(rank) * C::kCtaM;
         const int b_row = nb * BN + int(rank) * C::kBRows;
+        const int sfb_block0 = (nb * BN) / 128;
 #pragma unroll 1
         for (int ks = 0; ks < p.num_kstages; ++ks) {
           if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, ctl)) {
@@ -294,14 +306,14 @@ __global__ void __launch_bounds__(384, 1)
           ptx::tma_load_2d<CG>(stage_a(stage), &tmA, kx, a_row, fb, pol_a);
           ptx::tma_load_2d<CG>(stage_b(stage), &tmB, kx, b_row, fb, pol_b);
           if constexpr (C::kScaled) {
-            const int atom0 = ks * FmtTraits<FMT>::kSfAtoms;
-            // SFA: this CTA's 128 rows = scale row-block (a_row / 128)
+            const int atom0 = ks * T::kSfAtoms;
+            // SFA: this CTA's 128 rows = scale block (a_row / 128)
             ptx::tma_load_3d<CG>(stage_sfa(stage), &tmSFA, 0, atom0, a_row / 128, fb, pol_a);
-            // SFB: the whole N tile, every CTA of the pair holds a copy
+            // SFB: every CTA of the pair holds the whole N tile's scales
 #pragma unroll
-            for (int rb = 0; rb < BN / 128; ++rb)
-              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(rb * FmtTraits<FMT>::kSfAtoms * 512), &tmSFB, 0,
-                                   atom0, nb * (BN / 128) + rb, fb, pol_b);
+            for (int a = 0; a < C::kSfbBlocks; ++a)
+              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(a * T::kSfAtoms * 512), &tmSFB, 0, atom0,
+                                   sfb_block0 + a, fb, pol_b);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -311,15 +323,12 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok && leader) {
         // drain: every armed stage completes once its bytes land
+        Ctl quiet = ctl;
+        int dummy = 0;
+        quiet.abort_flag = &dummy;   // keep waiting through the abort, still bounded
 #pragma unroll 1
-        for (int s = 0; s < STAGES; ++s) {
-          if (armed & (1u << s)) {
-            Ctl quiet = ctl;
-            int dummy = 0;
-            quiet.abort_flag = &dummy;   // keep waiting through the abort, still bounded
-            wait_bar<false>(full_bar(s), (armed_par >> s) & 1u, quiet);
-          }
-        }
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) wait_bar<false>(full_bar(s), (armed_par >> s) & 1u, quiet);
       }
     }
     __syncwarp();
@@ -328,6 +337,7 @@ __global__ void __launch_bounds__(384, 1)
   else if (warp == 1) {
     if (leader && ptx::elect_one()) {
       uint32_t stage = 0, phase = 0, acc = 0, accph = 0;
+      uint32_t region = 0;        // next scale region in tensor memory (ring of kRegions)
       bool ok = true;
       if (p.inject_stall) ok = wait_bar<false>(never_bar, 0u, ctl);
       const uint16_t mask = (CG == 2) ? uint16_t(0x3) : uint16_t(0x1);
@@ -345,37 +355,38 @@ __global__ void __launch_bounds__(384, 1)
             ok = false;
             break;
           }
-          const uint32_t slot = tmem + uint32_t(C::kScaleBase + stage * C::kSlotCols);
-          if constexpr (C::kScaled) {
-            // scales -> tensor memory, same thread as the MMAs that read them
-#pragma unroll
-            for (int g = 0; g < FmtTraits<FMT>::kSfAtoms; ++g) {
-              ptx::tmem_cp_32x128b_x4<CG>(slot + uint32_t(4 * g), sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));
-#pragma unroll
-              for (int rb = 0; rb < BN / 128; ++rb)
-                ptx::tmem_cp_32x128b_x4<CG>(
-                    slot + uint32_t(C::kSfaCols + g * (BN / 128) * 4 + rb * 4),
-                    sdesc_sf(stage_sfb(stage) + uint32_t(rb * FmtTraits<FMT>::kSfAtoms * 512 + 512 * g)));
-            }
-          }
           const uint64_t adesc = sdesc_sw128(stage_a(stage));
           const uint64_t bdesc = sdesc_sw128(stage_b(stage));
 #pragma unroll
           for (int j = 0; j < C::kMmasPerStage; ++j) {
-            const int k0 = ks * FmtTraits<FMT>::kStageK + j * FmtTraits<FMT>::kMmaK;
-            if (k0 < p.k) {
-              const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
-              const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
-              if constexpr (FMT == FMT_BF16) {
-                ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, accum);
-              } else if constexpr (FMT == FMT_MXFP8) {
-                // one atom per stage; MMA j reads byte j of each scale word
+            const int k0 = ks * T::kStageK + j * T::kMmaK;
+            if (k0 >= p.k) break;
+            const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
+            const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
+            if constexpr (FMT == FMT_BF16) {
+              ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, accum);
+            } else {
+              // scales -> tensor memory from this thread, right before the MMAs that
+              // read them: one region per stage (MXFP8: MMA j reads byte j of each
+              // word) or per MMA (NVFP4: MMA j reads atom j)
+              const int g = (FMT == FMT_NVFP4) ? j : 0;
+              if (FMT == FMT_NVFP4 || j == 0) {
+                const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
+                ptx::tmem_cp_32x128b_x4<CG>(reg, sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));
+#pragma unroll
+                for (int a = 0; a < C::kSfbBlocks; ++a)
+                  ptx::tmem_cp_32x128b_x4<CG>(reg + uint32_t(4 + 4 * a),
+                                              sdesc_sf(stage_sfb(stage) + uint32_t((a * T::kSfAtoms + g) * 512)));
+              }
+              const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
+              if constexpr (FMT == FMT_MXFP8) {
                 const uint32_t idesc = C::kIdescBase | (uint32_t(j) << 29) | (uint32_t(j) << 4);
-                ptx::mma_mxf8<CG>(d_tmem, adesc + koff, bdesc + koff, idesc, slot, slot + C::kSfaCols, accum);
+                ptx::mma_mxf8<CG>(d_tmem, adesc + koff, bdesc + koff, idesc, reg, reg + 4u, accum);
               } else {
-                // four atoms per stage; MMA j reads atom j (all four bytes)
-                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, slot + uint32_t(4 * j),
-                                  slot + uint32_t(C::kSfaCols + j * (BN / 128) * 4), accum);
+                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, reg, reg + 4u, accum);
+              }
+              if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= p.k) {
+                if (++region == uint32_t(C::kRegions)) region = 0;
               }
             }
           }
@@ -405,8 +416,11 @@ __global__ void __launch_bounds__(384, 1)
   else if (warp >= 4) {
     const int e = warp - 4;
     const int q = warp & 3;              // accumulator lane quadrant this warp may read
-    const int h = e >> 2;                // column half
-    const uint32_t my_buf0 = epi_base + uint32_t(e * 2 * C::kEpiBufBytes);
+    const int h = e >> 2;                // column half: [0, 128) or [128, BN)
+    constexpr int kChunksLo = 4;
+    constexpr int kChunksHi = BN / 32 - 4;
+    const int nch = h == 0 ? kChunksLo : kChunksHi;
+    const uint32_t my_buf0 = epi_base + uint32_t(e * C::kEpiBufs * C::kEpiBufBytes);
     const uint32_t acce_lead0 = (CG == 2) ? ptx::map_to_rank(acce_bar(0), 0) : acce_bar(0);
     float alpha = p.alpha;
     if (p.ta) alpha = alpha * __ldg(p.ta);
@@ -421,25 +435,44 @@ __global__ void __launch_bounds__(384, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      constexpr int kChunks = BN / 2 / 32;
-      uint32_t v[kChunks][32];
-      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
+      uint32_t v[4][32];
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * 128);
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v[c]);
+      for (int c = 0; c < 4; ++c)
+        if (c < nch) ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v[c]);
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(acce_lead0 + 8u * acc);
+      if (lane == 0) {
+        // Accumulator buffer free.  The loads above have completed (wait::ld),
+        // so only the signal has to reach the MMA issuer: leader warps arrive
+        // on it directly; each follower warp sends a 16-byte async copy whose
+        // completion the leader's warp of the same index expects on the same
+        // barrier.  (A cluster-scope release arrive costs a cluster-wide fence.)
+        if (CG == 1) {
+          ptx::mbar_arrive(acce_bar(acc));
+        } else if (leader) {
+          ptx::mbar_arrive_expect_tx(acce_bar(acc), 16u);
+        } else {
+          ptx::bulk_copy_to_cluster(ptx::map_to_rank(epi_sig_slot(e), 0), epi_sig_slot(e), 16u, acce_lead0 + 8u * acc);
+        }
+      }
       if (++acc == ACC) {
         acc = 0;
         accph ^= 1u;
       }
       const int row0 = mb * C::kMmaM + int(rank) * C::kCtaM + q * 32;
-      const int col0 = nb * BN + h * (BN / 2);
+      const int col0 = nb * BN + h * 128;
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint32_t buf = my_buf0 + uint32_t((c & 1) * C::kEpiBufBytes);
-        if (lane == 0) ptx::bulk_wait_group_read<1>();
+      for (int c = 0; c < 4; ++c) {
+        if (c >= nch) break;
+        const uint32_t buf = my_buf0 + uint32_t((C::kEpiBufs == 2 ? (c & 1) : 0) * C::kEpiBufBytes);
+        if (lane == 0) {
+          if (C::kEpiBufs == 2)
+            ptx::bulk_wait_group_read<1>();
+          else
+            ptx::bulk_wait_group_read<0>();
+        }
         __syncwarp();
         const uint32_t row_addr = buf + uint32_t(lane * 64);
 #pragma unroll

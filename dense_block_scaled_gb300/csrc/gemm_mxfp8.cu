@@ -5,10 +5,13 @@
 namespace tkg {
 
 tkg_status launch_mxfp8(const Problem& pr, cudaStream_t s) {
+  // One 256-column accumulator: tensor memory (512 columns) cannot hold two
+  // next to the scale regions.  The epilogue frees it as soon as it is in
+  // registers, so the next tile's MMAs wait only for that drain.
   const int cg = option(TKG_OPT_CTA_GROUP);
   if (option(TKG_OPT_SINGLE_STAGE)) return launch_gemm<FMT_MXFP8, 2, 256, 1, 1>(pr, s);
-  if (cg == 1) return launch_gemm<FMT_MXFP8, 1, 256, 3, 1>(pr, s);
-  return launch_gemm<FMT_MXFP8, 2, 256, 5, 1>(pr, s);
+  if (cg == 1) return launch_gemm<FMT_MXFP8, 1, 256, 4, 1>(pr, s);
+  return launch_gemm<FMT_MXFP8, 2, 256, 6, 1>(pr, s);
 }
 
 }  // namespace tkg
