@@ -6,10 +6,10 @@ namespace tkg {
 
 tkg_status launch_bf16(const Problem& pr, cudaStream_t s) {
   const int cg = option(TKG_OPT_CTA_GROUP);
-  if (option(TKG_OPT_SINGLE_STAGE)) return launch_gemm<FMT_BF16, 2, 256, 1, 2>(pr, s);
-  if (cg == 1) return launch_gemm<FMT_BF16, 1, 256, 4, 2>(pr, s);
-  if (option(TKG_OPT_ACC_STAGES) == 1) return launch_gemm<FMT_BF16, 2, 256, 6, 1>(pr, s);
-  return launch_gemm<FMT_BF16, 2, 256, 6, 2>(pr, s);
+  if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_BF16, 2, 256, 1, 2>(pr, s);
+  if (cg == 1) return launch_sched<FMT_BF16, 1, 256, 4, 2>(pr, s);
+  if (option(TKG_OPT_ACC_STAGES) == 1) return launch_sched<FMT_BF16, 2, 256, 6, 1>(pr, s);
+  return launch_sched<FMT_BF16, 2, 256, 6, 2>(pr, s);
 }
 
 }  // namespace tkg

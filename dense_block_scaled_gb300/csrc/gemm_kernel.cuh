@@ -109,7 +109,9 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   nb = r / gm;
 }
 
-template <int FMT, int CG, int BN, int STAGES, int ACC>
+enum : int { SCHED_STATIC = 0, SCHED_CLC = 1 };
+
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC>
 struct GemmConfig {
   using T = FmtTraits<FMT>;
   static constexpr bool kScaled = FMT != FMT_BF16;
@@ -129,8 +131,13 @@ struct GemmConfig {
   static constexpr int kStageBytes = ((kABytes + kBBytes + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
   static constexpr int kMmasPerStage = T::kStageK / T::kMmaK;
   static constexpr int kEpiBufBytes = 32 * 64;      // 32 rows x 32 BF16
-  static constexpr int kNumBars = 2 * STAGES + 2 * ACC + 2;
-  static constexpr int kFixedBytes = kNumBars * 8 + kEpiWarps * 16 + 16 + 1024;   // barriers, signal slots, slack
+  static constexpr int kNumBars = 2 * STAGES + 2 * ACC + 2 + 4;
+  // barriers, epilogue signal slots, two tile-scheduler answers, alignment slack
+  static constexpr int kFixedBytes = kNumBars * 8 + (kEpiWarps + 2) * 16 + 16 + 1024;
+  static constexpr bool kClc = SCHED == SCHED_CLC;
+  // arrivals that free one scheduler answer: producer, epilogue warps, per CTA;
+  // plus the MMA issuer and the scheduler itself in the pair leader
+  static constexpr int kClcConsumers = CG * (1 + kEpiWarps) + 2;
   // two staging buffers per epilogue warp when they fit, else one
   static constexpr int kEpiBufs =
       STAGES * kStageBytes + kEpiWarps * 2 * kEpiBufBytes + kFixedBytes <= 232448 ? 2 : 1;
@@ -193,12 +200,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
   }
 }
 
-template <int FMT, int CG, int BN, int STAGES, int ACC>
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC>
 __global__ void __launch_bounds__(384, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
-  using C = GemmConfig<FMT, CG, BN, STAGES, ACC>;
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -227,8 +234,11 @@ __global__ void __launch_bounds__(384, 1)
   auto acce_bar = [&](int a) { return bars + uint32_t(8 * (2 * STAGES + ACC + a)); };
   const uint32_t drain_bar = bars + uint32_t(8 * (2 * STAGES + 2 * ACC));
   const uint32_t never_bar = drain_bar + 8;
+  auto clc_full = [&](uint32_t i) { return never_bar + 8u + 8u * i; };     // answer i landed
+  auto clc_empty = [&](uint32_t i) { return never_bar + 24u + 8u * i; };   // answer i read by all (leader)
   // 16-byte landing slots for the follower's "accumulator free" signals (epilogue)
-  auto epi_sig_slot = [&](int w) { return ((never_bar + 8u + 15u) & ~15u) + uint32_t(16 * w); };
+  auto epi_sig_slot = [&](int w) { return ((never_bar + 40u + 15u) & ~15u) + uint32_t(16 * w); };
+  auto clc_resp = [&](uint32_t i) { return epi_sig_slot(C::kEpiWarps) + 16u * i; };
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -242,6 +252,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     ptx::mbar_init(drain_bar, 1);
     ptx::mbar_init(never_bar, 1);
+    for (uint32_t i = 0; i < 2; ++i) {
+      ptx::mbar_init(clc_full(i), 1);
+      ptx::mbar_init(clc_empty(i), C::kClcConsumers);
+    }
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
@@ -271,6 +285,33 @@ __global__ void __launch_bounds__(384, 1)
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
 
+  // Next tile for this cluster.  Static: a fixed stride over the tile list.
+  // Cluster launch control: the grid holds one cluster per tile; a running
+  // cluster takes over a cluster that has not started yet (its tile is that
+  // cluster's index).  The pair leader's scheduler lane asks; every role reads
+  // the answer from its own CTA's copy and releases it.  Returns -1 when no
+  // tile is left, -2 when the kernel is aborting.
+  auto next_tile = [&](int t, uint32_t& cslot, uint32_t& cphase) -> int {
+    if constexpr (!C::kClc) {
+      (void)cslot;
+      (void)cphase;
+      return t + num_clusters < p.num_tiles ? t + num_clusters : -1;
+    } else {
+      if (!wait_bar<false>(clc_full(cslot), cphase, ctl)) return -2;
+      uint32_t x = 0;
+      const bool got = ptx::clc_read(clc_resp(cslot), x);
+      if (leader)
+        ptx::mbar_arrive(clc_empty(cslot));
+      else
+        ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(clc_empty(cslot), 0));
+      if (++cslot == 2) {
+        cslot = 0;
+        cphase ^= 1u;
+      }
+      return got ? int(x) / CG : -1;
+    }
+  };
+
   // ------------------------------------------------------------------ producer
   if (warp == 0) {
     if (ptx::elect_one()) {
@@ -282,8 +323,9 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t armed = 0;          // stages whose last arming is not yet known complete
       uint32_t armed_par = 0;      // parity of that arming
       bool ok = true;
+      uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      for (int t = cluster_id; t >= 0 && ok;) {
         int mb, nb;
         tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
         const int a_row = mb * C::kMmaM + int(rank) * C::kCtaM;
@@ -320,6 +362,9 @@ __global__ void __launch_bounds__(384, 1)
             phase ^= 1u;
           }
         }
+        if (!ok) break;
+        t = next_tile(t, cslot, cphase);
+        if (t == -2) ok = false;
       }
       if (!ok && leader) {
         // drain: every armed stage completes once its bytes land
@@ -341,8 +386,9 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       if (p.inject_stall) ok = wait_bar<false>(never_bar, 0u, ctl);
       const uint16_t mask = (CG == 2) ? uint16_t(0x3) : uint16_t(0x1);
+      uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      for (int t = cluster_id; t >= 0 && ok;) {
         if (!wait_bar<CG == 2>(acce_bar(acc), accph ^ 1u, ctl)) {
           ok = false;
           break;
@@ -402,6 +448,8 @@ __global__ void __launch_bounds__(384, 1)
           acc = 0;
           accph ^= 1u;
         }
+        t = next_tile(t, cslot, cphase);
+        if (t == -2) ok = false;
       }
       // every MMA this thread issued has finished before tensor memory goes away
       ptx::tc_commit<CG>(drain_bar, uint16_t(1u << rank));
@@ -409,6 +457,33 @@ __global__ void __launch_bounds__(384, 1)
       int dummy = 0;
       quiet.abort_flag = &dummy;
       wait_bar<false>(drain_bar, 0u, quiet);
+    }
+    __syncwarp();
+  }
+  // ------------------------------------------------------------------ tile scheduler
+  else if (warp == 2) {
+    if constexpr (C::kClc) {
+      if (leader && ptx::elect_one()) {
+        uint32_t slot = 0, ph = 0;
+#pragma unroll 1
+        while (true) {
+          // the answer slot is free once every role has read its last answer
+          if (!wait_bar<CG == 2>(clc_empty(slot), ph ^ 1u, ctl)) break;
+          ptx::mbar_arrive_expect_tx(clc_full(slot), 16u);
+          if (CG == 2) ptx::mbar_expect_tx_relaxed_cluster(ptx::map_to_rank(clc_full(slot), 1), 16u);
+          ptx::clc_try_cancel<CG == 2>(clc_resp(slot), clc_full(slot));
+          // read the answer too: a failed request ends the schedule
+          if (!wait_bar<false>(clc_full(slot), ph, ctl)) break;
+          uint32_t x = 0;
+          const bool got = ptx::clc_read(clc_resp(slot), x);
+          ptx::mbar_arrive(clc_empty(slot));
+          if (++slot == 2) {
+            slot = 0;
+            ph ^= 1u;
+          }
+          if (!got) break;
+        }
+      }
     }
     __syncwarp();
   }
@@ -426,8 +501,9 @@ __global__ void __launch_bounds__(384, 1)
     if (p.ta) alpha = alpha * __ldg(p.ta);
     if (p.tb) alpha = alpha * __ldg(p.tb);
     uint32_t acc = 0, accph = 0;
+    uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    for (int t = cluster_id; t >= 0;) {
       int mb, nb;
       tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
       uint32_t ok = 0;
@@ -494,6 +570,9 @@ __global__ void __launch_bounds__(384, 1)
           ptx::bulk_commit_group();
         }
       }
+      int nt = 0;
+      if (lane == 0) nt = next_tile(t, cslot, cphase);
+      t = __shfl_sync(0xffffffffu, nt, 0);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();

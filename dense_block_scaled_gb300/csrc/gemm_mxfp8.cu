@@ -9,9 +9,9 @@ tkg_status launch_mxfp8(const Problem& pr, cudaStream_t s) {
   // next to the scale regions.  The epilogue frees it as soon as it is in
   // registers, so the next tile's MMAs wait only for that drain.
   const int cg = option(TKG_OPT_CTA_GROUP);
-  if (option(TKG_OPT_SINGLE_STAGE)) return launch_gemm<FMT_MXFP8, 2, 256, 1, 1>(pr, s);
-  if (cg == 1) return launch_gemm<FMT_MXFP8, 1, 256, 4, 1>(pr, s);
-  return launch_gemm<FMT_MXFP8, 2, 256, 6, 1>(pr, s);
+  if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_MXFP8, 2, 256, 1, 1>(pr, s);
+  if (cg == 1) return launch_sched<FMT_MXFP8, 1, 256, 4, 1>(pr, s);
+  return launch_sched<FMT_MXFP8, 2, 256, 6, 1>(pr, s);
 }
 
 }  // namespace tkg

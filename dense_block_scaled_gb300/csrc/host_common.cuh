@@ -40,11 +40,11 @@ tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Launch one instantiation of the persistent GEMM.
-template <int FMT, int CG, int BN, int STAGES, int ACC>
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED>
 tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
-  using C = GemmConfig<FMT, CG, BN, STAGES, ACC>;
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
-  auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC>;
+  auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC, SCHED>;
   // Request at least just over half an SM's shared memory so that no two CTAs
   // ever share an SM: each allocates all 512 tensor-memory columns.
   constexpr int kLaunchSmem = C::kSmemBytes > 118784 ? C::kSmemBytes : 118784;
@@ -144,6 +144,9 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   int clusters = max_clusters < p.num_tiles ? max_clusters : p.num_tiles;
   const int cap = option(TKG_OPT_MAX_CLUSTERS);
   if (cap > 0 && clusters > cap) clusters = cap;
+  // cluster launch control: one cluster per tile; running clusters take over
+  // the ones that have not started
+  if (SCHED == SCHED_CLC) clusters = p.num_tiles;
   cfg.gridDim = dim3(clusters * CG, 1, 1);
 
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p);
@@ -152,6 +155,13 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
     return TKG_ERR_CUDA;
   }
   return TKG_OK;
+}
+
+// Cluster launch control unless TKG_OPT_SCHEDULER asks for the static schedule.
+template <int FMT, int CG, int BN, int STAGES, int ACC>
+tkg_status launch_sched(const Problem& pr, cudaStream_t s) {
+  if (option(TKG_OPT_SCHEDULER) == 1) return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC>(pr, s);
+  return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_CLC>(pr, s);
 }
 
 tkg_status launch_bf16(const Problem& pr, cudaStream_t s);

@@ -91,6 +91,54 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Relaxed arrive on a barrier of another CTA of the cluster (no ordering of
+// prior memory operations: only for signals that publish no data).
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_relaxed_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Ask to cancel a cluster of this grid that has not started; its 16-byte
+// answer lands at `resp` (in every CTA of the cluster when MULTICAST) and
+// completes 16 transaction bytes on `bar` (same offset in every CTA).
+template <bool MULTICAST>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  if constexpr (MULTICAST)
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+        "[%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+  else
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     resp),
+                 "r"(bar)
+                 : "memory");
+}
+
+// Reads an answer: returns true and the first CTA index (x) of the cancelled
+// cluster, or false when no cluster was left to cancel.
+__device__ __forceinline__ bool clc_read(uint32_t resp, uint32_t& first_ctaid_x) {
+  uint32_t ok = 0, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  first_ctaid_x = x;
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- cluster barrier
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

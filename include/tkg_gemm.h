@@ -156,7 +156,10 @@ typedef enum {
   TKG_OPT_INJECT_STALL = 4,   /* 1: the MMA role waits on a barrier nothing arrives on
                                   (test of the timeout path; output is garbage) */
   TKG_OPT_MAX_CLUSTERS = 5,   /* cap on persistent clusters (0: fill the GPU) */
-  TKG_OPT_ACC_STAGES = 6      /* BF16 only: 1 = single accumulator buffer (0: double) */
+  TKG_OPT_ACC_STAGES = 6,     /* BF16 only: 1 = single accumulator buffer (0: double) */
+  TKG_OPT_SCHEDULER = 7       /* 0: cluster launch control (one cluster per tile, running
+                                  clusters take over pending ones); 1: static persistent
+                                  grid (TKG_OPT_MAX_CLUSTERS applies only here) */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);

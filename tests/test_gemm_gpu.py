@@ -15,14 +15,16 @@ pytestmark = pytest.mark.gpu
 FMTS = ["bf16", "mxfp8", "nvfp4"]
 
 
+ALL_OPTIONS = (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
+               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER)
+
+
 @pytest.fixture(autouse=True)
 def _reset_options():
-    for o in (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
-              tkg.OPT_MAX_CLUSTERS):
+    for o in ALL_OPTIONS:
         tkg.set_option(o, 0)
     yield
-    for o in (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
-              tkg.OPT_MAX_CLUSTERS):
+    for o in ALL_OPTIONS:
         tkg.set_option(o, 0)
 
 
@@ -60,10 +62,27 @@ def test_bf16_odd_k():
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_many_tiles_per_cta(fmt):
-    # few persistent clusters: every CTA walks many tiles, the stage and
-    # accumulator phases wrap many times
+    # static schedule on few persistent clusters: every CTA walks many tiles,
+    # the stage and accumulator phases wrap many times
+    tkg.set_option(tkg.OPT_SCHEDULER, 1)
     tkg.set_option(tkg.OPT_MAX_CLUSTERS, 3)
     _check(fmt, 1024, 1024, 512, seed=9)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_launch_control_equals_static_schedule(fmt):
+    # cluster launch control and the static schedule compute every tile the
+    # same way: identical bits; many more tiles than resident clusters
+    m, n, k = 4096, 2048, 512
+    ops = Operands(fmt, m, n, k, seed=14)
+    dev = ops.upload()
+    D_clc = run_gemm(fmt, dev, m, n, k, 1.0)
+    tkg.set_option(tkg.OPT_SCHEDULER, 1)
+    D_static = run_gemm(fmt, dev, m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    assert torch.equal(D_clc.view(torch.int16), D_static.view(torch.int16))
+    ref, S = ops.reference(rows=(m - 300, 300))
+    assert_within_tolerance(bf16_to_f64(D_clc[m - 300:]), ref, S, "launch control")
 
 
 @pytest.mark.parametrize("fmt", FMTS)
