@@ -235,6 +235,29 @@ def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flu
     return ms / 1e3 / steps
 
 
+def graph_seconds(w, steps, torch, tkg):
+    """Seconds per launch when the K launches are replayed from one captured CUDA
+    graph: the same kernels without the per-call host work."""
+    w.launch(0, tkg)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(steps):
+            w.launch(i, tkg)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    e1.synchronize()
+    st = tkg.device_status()
+    if st != tkg.OK:
+        raise RuntimeError(f"device status after graph replay: {tkg.status_string(st)}")
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
 def e2e_seconds(w, steps, torch, tkg):
     """Per-step seconds through the public API with HOST buffers: pinned inputs
     copied to the device, the GEMM, the output copied back, all timed."""
@@ -394,20 +417,24 @@ def run_ours(args):
         for s in [int(x) for x in args.sweep.split(",") if x]:
             w = Workload("bf16", s, SEEDS["bf16"], l2, torch, tkg, synth)
             t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+            tg = graph_seconds(w, args.steps, torch, tkg)
             sweep[str(s)] = {"tflops": w.flop / t / 1e12, "us": t * 1e6, "input_groups": w.groups,
-                             "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS["bf16"]}
+                             "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS["bf16"],
+                             "us_graph": tg * 1e6, "tflops_graph": w.flop / tg / 1e12}
             del w
             torch.cuda.empty_cache()
         for fmt in ("bf16", "nvfp4"):
             for mm in [int(x) for x in args.skinny.split(",") if x]:
                 w = Workload(fmt, 8192, 1004, l2, torch, tkg, synth, mnk=(mm, 8192, 8192))
                 t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+                tg = graph_seconds(w, args.steps, torch, tkg)
                 byts = w.in_bytes + w.out_bytes
                 tf = w.flop / t / 1e12
                 roof = min(PAGES_PEAK_TFLOPS[fmt], w.flop / byts * pk["hbm_gbs"] / 1e3)
                 skinny[f"{fmt} M={mm} N=K=8192"] = {
                     "us": t * 1e6, "tflops": tf, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / pk["hbm_gbs"],
-                    "roofline_tflops": roof, "frac_of_roofline": tf / roof, "input_groups": w.groups}
+                    "roofline_tflops": roof, "frac_of_roofline": tf / roof, "input_groups": w.groups,
+                    "us_graph": tg * 1e6, "frac_of_roofline_graph": w.flop / tg / 1e12 / roof}
                 del w
                 torch.cuda.empty_cache()
         if not args.no_e2e:

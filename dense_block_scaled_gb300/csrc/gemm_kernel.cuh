@@ -165,15 +165,19 @@ struct GemmConfig {
 
 struct Ctl {
   volatile int* abort_flag;   // this CTA's flag (shared memory)
-  uint32_t peer_abort;        // shared::cluster address of the peer's flag (CG == 2)
+  uint32_t abort_smem;        // its shared-memory address (same offset in every CTA)
+  uint32_t rank;              // this CTA's rank in the cluster
+  uint32_t ncta;              // CTAs in the cluster
   unsigned int* status;
   unsigned long long timeout_ns;
-  int cg;
 };
 
+// Mark the kernel as aborting: this CTA's flag, every other CTA of the
+// cluster, and the device status word the host reads.
 __device__ __forceinline__ void raise_abort(const Ctl& c) {
   *c.abort_flag = 1;
-  if (c.cg == 2) ptx::st_shared_cluster_u32(c.peer_abort, 1u);
+  for (uint32_t r = 0; r < c.ncta; ++r)
+    if (r != c.rank) ptx::st_shared_cluster_u32(ptx::map_to_rank(c.abort_smem, r), 1u);
   atomicOr(c.status, DEV_ERR_TIMEOUT);
 }
 
@@ -274,13 +278,19 @@ __global__ void __launch_bounds__(384, 1)
   if (CG == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  // Programmatic dependent launch: the set-up above overlapped the previous
+  // kernel's tail; global memory is touched only after it has completed.  The
+  // next kernel may start its own set-up as soon as SMs free up.
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
 
   Ctl ctl;
   ctl.abort_flag = &s_abort;
-  ctl.peer_abort = (CG == 2) ? ptx::map_to_rank(ptx::smem_u32(&s_abort), rank ^ 1u) : 0u;
+  ctl.abort_smem = ptx::smem_u32(&s_abort);
+  ctl.rank = rank;
+  ctl.ncta = CG;
   ctl.status = p.status;
   ctl.timeout_ns = p.timeout_ns;
-  ctl.cg = CG;
 
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;

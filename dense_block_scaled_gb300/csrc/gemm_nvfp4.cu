@@ -9,6 +9,10 @@ tkg_status launch_nvfp4(const Problem& pr, cudaStream_t s) {
   // next to the scale regions.  The epilogue frees it as soon as it is in
   // registers, so the next tile's MMAs wait only for that drain.
   const int cg = option(TKG_OPT_CTA_GROUP);
+  // few output tiles (skinny M): split K across a cluster
+  const int split = choose_split(pr, FmtTraits<FMT_NVFP4>::kStageK);
+  if (split == 2) return launch_splitk<FMT_NVFP4, 2, 5>(pr, s);
+  if (split == 3) return launch_splitk<FMT_NVFP4, 3, 5>(pr, s);
   if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_NVFP4, 2, 256, 1, 1>(pr, s);
   if (cg == 1) return launch_sched<FMT_NVFP4, 1, 256, 3, 1>(pr, s);
   return launch_sched<FMT_NVFP4, 2, 256, 5, 1>(pr, s);

@@ -1,0 +1,340 @@
+// gemm_splitk.cuh -- split-K GEMM for problems with few output tiles (skinny M).
+//
+// A GEMM with M = 16 or 128 and N = K = 8192 has only 64 output tiles of
+// 128 x 128, fewer than half the SMs, and is bound by HBM reads of B.  Here a
+// cluster of SPLIT CTAs works on one 128 x 128 tile, each CTA on its own
+// stretch of K, so SPLIT times as many SMs stream B.  The partial
+// accumulators meet in the cluster leader's shared memory (distributed shared
+// memory, no global scratch): once every CTA's MMAs are done, the others write
+// their FP32 partials into the leader's now idle stage buffers, and the leader
+// adds them, scales by alpha, rounds to BF16 and stores D.
+//
+// Same operand formats, layouts, roles and bounded waits as gemm_kernel.cuh;
+// single-CTA MMAs (M = 128, N = 128) and one tile per cluster.
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace tkg {
+
+template <int FMT, int SPLIT, int STAGES>
+struct SplitKConfig {
+  using T = FmtTraits<FMT>;
+  static constexpr bool kScaled = FMT != FMT_BF16;
+  static constexpr int kThreads = 384;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int kRowBytes = 128;
+  static constexpr int kABytes = BM * kRowBytes;
+  static constexpr int kBBytes = BN * kRowBytes;
+  static constexpr int kSfaBytes = T::kSfAtoms * 512;
+  static constexpr int kSfbBytes = T::kSfAtoms * 512;   // one 128-row scale block
+  static constexpr int kStageBytes = ((kABytes + kBBytes + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
+  static constexpr int kMmasPerStage = T::kStageK / T::kMmaK;
+  static constexpr int kEpiBufBytes = 32 * 64;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kPartialBytes = BM * BN * 4;   // one CTA's FP32 accumulator
+  static constexpr int kNumBars = 2 * STAGES + 3;
+  static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
+  static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kTxBytes = uint32_t(kABytes + kBBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
+  static constexpr int kAccCols = BN;
+  static constexpr int kScaleBase = BN;
+  static constexpr int kRegionCols = 8;                  // 4 columns of A scales, 4 of B scales
+  static constexpr int kRegions = (512 - BN) / kRegionCols;
+  static constexpr int kTmemCols = 512;
+  static_assert(SPLIT >= 1 && SPLIT <= 4, "split factor");
+  static_assert((SPLIT - 1) * kPartialBytes <= STAGES * kStageBytes, "partials must fit the stage buffers");
+  static_assert(kSmemBytes <= 232448, "shared memory overflow");
+  static constexpr uint32_t kIdesc =
+      FMT == FMT_BF16 ? idesc_f16(BM, BN)
+                      : idesc_bs(BM, BN, FMT == FMT_NVFP4 ? 1u : 0u, FMT == FMT_MXFP8 ? 1u : 0u, 0u, 0u);
+};
+
+template <int FMT, int SPLIT, int STAGES>
+__global__ void __launch_bounds__(384, 1)
+    gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                       const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  using C = SplitKConfig<FMT, SPLIT, STAGES>;
+  using T = FmtTraits<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = (SPLIT > 1) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  auto stage_a = [&](int s) { return base + uint32_t(s * C::kStageBytes); };
+  auto stage_b = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes); };
+  auto stage_sfa = [&](int s) { return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes); };
+  auto stage_sfb = [&](int s) {
+    return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes + C::kSfaBytes);
+  };
+  const uint32_t epi_base = base + uint32_t(STAGES * C::kStageBytes);
+  const uint32_t bars = base + uint32_t(C::kBarOffset);
+  auto full_bar = [&](int s) { return bars + uint32_t(8 * s); };
+  auto empty_bar = [&](int s) { return bars + uint32_t(8 * (STAGES + s)); };
+  const uint32_t accf_bar = bars + uint32_t(8 * (2 * STAGES));
+  const uint32_t drain_bar = accf_bar + 8;
+  const uint32_t never_bar = drain_bar + 8;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    ptx::mbar_init(accf_bar, 1);
+    ptx::mbar_init(drain_bar, 1);
+    ptx::mbar_init(never_bar, 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmD);
+    if (C::kScaled) {
+      ptx::prefetch_tmap(&tmSFA);
+      ptx::prefetch_tmap(&tmSFB);
+    }
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc<1>(ptx::smem_u32(&s_tmem_base), C::kTmemCols);
+    ptx::tmem_relinquish<1>();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (SPLIT > 1) ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+  // Programmatic dependent launch: the set-up above overlapped the previous
+  // kernel's tail; global memory is touched only after it has completed.  The
+  // next kernel may start its own set-up as soon as SMs free up.
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+
+  Ctl ctl;
+  ctl.abort_flag = &s_abort;
+  ctl.abort_smem = ptx::smem_u32(&s_abort);
+  ctl.rank = rank;
+  ctl.ncta = SPLIT;
+  ctl.status = p.status;
+  ctl.timeout_ns = p.timeout_ns;
+
+  int mb, nb;
+  tile_coords(int(blockIdx.x) / SPLIT, p.tiles_m, p.tiles_n, mb, nb);
+  // this CTA's stretch of K (in stages); the host keeps every stretch non-empty
+  const int per = (p.num_kstages + SPLIT - 1) / SPLIT;
+  const int ks0 = int(rank) * per;
+  const int ks1 = min(ks0 + per, p.num_kstages);
+
+  // ------------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      const uint64_t pol_a = ptx::policy_evict_last();
+      const uint64_t pol_b = ptx::policy_evict_normal();
+      uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int ks = ks0; ks < ks1; ++ks) {
+        if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, ctl)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+        armed |= 1u << stage;
+        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+        const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
+        ptx::tma_load_2d<1>(stage_a(stage), &tmA, kx, mb * C::BM, full_bar(stage), pol_a);
+        ptx::tma_load_2d<1>(stage_b(stage), &tmB, kx, nb * C::BN, full_bar(stage), pol_b);
+        if constexpr (C::kScaled) {
+          ptx::tma_load_3d<1>(stage_sfa(stage), &tmSFA, 0, ks * T::kSfAtoms, mb, full_bar(stage), pol_a);
+          ptx::tma_load_3d<1>(stage_sfb(stage), &tmSFB, 0, ks * T::kSfAtoms, nb, full_bar(stage), pol_b);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        Ctl quiet = ctl;
+        int dummy = 0;
+        quiet.abort_flag = &dummy;
+#pragma unroll 1
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) wait_bar<false>(full_bar(s), (armed_par >> s) & 1u, quiet);
+      }
+    }
+    __syncwarp();
+  }
+  // ------------------------------------------------------------------ MMA issuer
+  else if (warp == 1) {
+    if (ptx::elect_one()) {
+      uint32_t stage = 0, phase = 0, region = 0;
+      bool ok = true;
+      if (p.inject_stall) ok = wait_bar<false>(never_bar, 0u, ctl);
+#pragma unroll 1
+      for (int ks = ks0; ks < ks1 && ok; ++ks) {
+        if (!wait_bar<false>(full_bar(stage), phase, ctl)) {
+          ok = false;
+          break;
+        }
+        const uint64_t adesc = sdesc_sw128(stage_a(stage));
+        const uint64_t bdesc = sdesc_sw128(stage_b(stage));
+#pragma unroll
+        for (int j = 0; j < C::kMmasPerStage; ++j) {
+          const int k0 = ks * T::kStageK + j * T::kMmaK;
+          if (k0 >= p.k) break;
+          const uint64_t koff = uint64_t((j * 32) >> 4);
+          const uint32_t accum = (ks > ks0 || j > 0) ? 1u : 0u;
+          if constexpr (FMT == FMT_BF16) {
+            ptx::mma_f16<1>(tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
+          } else {
+            const int g = (FMT == FMT_NVFP4) ? j : 0;
+            const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
+            if (FMT == FMT_NVFP4 || j == 0) {
+              ptx::tmem_cp_32x128b_x4<1>(reg, sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));
+              ptx::tmem_cp_32x128b_x4<1>(reg + 4u, sdesc_sf(stage_sfb(stage) + uint32_t(512 * g)));
+            }
+            if constexpr (FMT == FMT_MXFP8) {
+              const uint32_t idesc = C::kIdesc | (uint32_t(j) << 29) | (uint32_t(j) << 4);
+              ptx::mma_mxf8<1>(tmem, adesc + koff, bdesc + koff, idesc, reg, reg + 4u, accum);
+            } else {
+              ptx::mma_nvf4<1>(tmem, adesc + koff, bdesc + koff, C::kIdesc, reg, reg + 4u, accum);
+            }
+            if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= p.k) {
+              if (++region == uint32_t(C::kRegions)) region = 0;
+            }
+          }
+        }
+        ptx::tc_commit<1>(empty_bar(stage), 1);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) ptx::tc_commit<1>(accf_bar, 1);
+      ptx::tc_commit<1>(drain_bar, 1);
+      Ctl quiet = ctl;
+      int dummy = 0;
+      quiet.abort_flag = &dummy;
+      wait_bar<false>(drain_bar, 0u, quiet);
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ epilogue: own partial into registers
+  const bool epi = warp >= 4;
+  const int e = warp - 4;
+  const int q = warp & 3;              // accumulator lane quadrant
+  const int h = e >> 2;                // column half: [0, 64) or [64, 128)
+  const int row = q * 32 + lane;       // tile row this thread holds
+  uint32_t v[2][32];
+  uint32_t have = 0;
+  if (epi) {
+    if (lane == 0) have = wait_bar<false>(accf_bar, 0u, ctl) ? 1u : 0u;
+    have = __shfl_sync(0xffffffffu, have, 0);
+    if (have) {
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(h * 64);
+      ptx::tmem_ld_32x32b_x32(taddr, v[0]);
+      ptx::tmem_ld_32x32b_x32(taddr + 32u, v[1]);
+      ptx::tmem_ld_wait();
+    }
+  }
+  // 16-byte chunk c (of 32 per 512-byte row) of a partial row, XOR-swizzled by row
+  auto partial_addr = [&](uint32_t region_base, int c) {
+    return region_base + uint32_t(row * 512) + uint32_t(((c ^ row) & 31) * 16);
+  };
+
+  // ------------------------------------------------------------------ split-K reduction
+  if constexpr (SPLIT > 1) {
+    // every CTA's MMAs are done, so the leader's stage buffers are free
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    if (epi && !leader && have) {
+      const uint32_t dst = ptx::map_to_rank(base + uint32_t((rank - 1) * C::kPartialBytes), 0);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t a = dst + uint32_t(row * 512) + uint32_t((((h * 16 + c * 8 + j) ^ row) & 31) * 16);
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v[c][4 * j]),
+                       "r"(v[c][4 * j + 1]), "r"(v[c][4 * j + 2]), "r"(v[c][4 * j + 3])
+                       : "memory");
+        }
+    }
+    ptx::cluster_sync();
+    if (epi && leader && have) {
+#pragma unroll 1
+      for (int r = 1; r < SPLIT; ++r) {
+        const uint32_t src = base + uint32_t((r - 1) * C::kPartialBytes);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(partial_addr(src, h * 16 + c * 8 + j)));
+            v[c][4 * j] = __float_as_uint(__uint_as_float(v[c][4 * j]) + __uint_as_float(w0));
+            v[c][4 * j + 1] = __float_as_uint(__uint_as_float(v[c][4 * j + 1]) + __uint_as_float(w1));
+            v[c][4 * j + 2] = __float_as_uint(__uint_as_float(v[c][4 * j + 2]) + __uint_as_float(w2));
+            v[c][4 * j + 3] = __float_as_uint(__uint_as_float(v[c][4 * j + 3]) + __uint_as_float(w3));
+          }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ epilogue: leader stores D
+  if (epi && leader && have && !s_abort) {
+    float alpha = p.alpha;
+    if (p.ta) alpha = alpha * __ldg(p.ta);
+    if (p.tb) alpha = alpha * __ldg(p.tb);
+    const uint32_t my_buf0 = epi_base + uint32_t(e * 2 * C::kEpiBufBytes);
+    const int row0 = mb * C::BM + q * 32;
+    const int col0 = nb * C::BN + h * 64;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t buf = my_buf0 + uint32_t(c * C::kEpiBufBytes);
+      const uint32_t row_addr = buf + uint32_t(lane * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          w[x] = ptx::pack_bf16x2(__uint_as_float(v[c][8 * j + 2 * x]) * alpha,
+                                  __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha);
+        ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ ((uint32_t(lane) >> 1) & 3u)) * 16u), w[0], w[1], w[2], w[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(&tmD, buf, col0 + c * 32, row0);
+        ptx::bulk_commit_group();
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (s_abort && threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 50000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (SPLIT > 1) ptx::cluster_sync();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc<1>(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace tkg

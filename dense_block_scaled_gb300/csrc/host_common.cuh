@@ -10,6 +10,7 @@
 
 #include "../../include/tkg_gemm.h"
 #include "gemm_kernel.cuh"
+#include "gemm_splitk.cuh"
 
 namespace tkg {
 
@@ -110,18 +111,21 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kLaunchSmem;
   cfg.stream = stream;
   int nattr = 0;
   if (CG == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = CG;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
   }
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
 
@@ -155,6 +159,104 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
     return TKG_ERR_CUDA;
   }
   return TKG_OK;
+}
+
+// Split-K launch: one cluster of SPLIT CTAs per 128 x 128 output tile.
+template <int FMT, int SPLIT, int STAGES>
+tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
+  using C = SplitKConfig<FMT, SPLIT, STAGES>;
+  using T = FmtTraits<FMT>;
+  auto kern = gemm_splitk_kernel<FMT, SPLIT, STAGES>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TKG_ERR_CUDA;
+  static bool attr_set[64] = {};
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return TKG_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  CUtensorMap tmA, tmB, tmSFA, tmSFB, tmD;
+  const bool bf16 = FMT == FMT_BF16;
+  const CUtensorMapDataType vt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t kdim = FMT == FMT_NVFP4 ? uint64_t(pr.k) / 2 : uint64_t(pr.k);
+  const uint64_t row_bytes = FMT == FMT_BF16 ? uint64_t(pr.k) * 2 : kdim;
+  const uint32_t boxk = bf16 ? 64 : 128;
+  tkg_status st;
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::BM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+    return st;
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::BN, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+    return st;
+  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
+    return st;
+  if constexpr (C::kScaled) {
+    const int bs = FMT == FMT_MXFP8 ? 32 : 16;
+    const int ka = ceil_div(ceil_div(pr.k, bs), 4);
+    if ((st = encode_3d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfa, 128, ka, ceil_div(pr.m, 128), 512,
+                        uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
+      return st;
+    if ((st = encode_3d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfb, 128, ka, ceil_div(pr.n, 128), 512,
+                        uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
+      return st;
+  } else {
+    tmSFA = tmD;
+    tmSFB = tmD;
+  }
+  GemmParams p;
+  p.m = pr.m;
+  p.n = pr.n;
+  p.k = pr.k;
+  p.num_kstages = ceil_div(pr.k, T::kStageK);
+  p.tiles_m = ceil_div(pr.m, C::BM);
+  p.tiles_n = ceil_div(pr.n, C::BN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.alpha = pr.alpha;
+  p.ta = pr.ta;
+  p.tb = pr.tb;
+  if ((st = device_status_word(&p.status)) != TKG_OK) return st;
+  const int tmo = option(TKG_OPT_TIMEOUT_MS);
+  p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
+  p.inject_stall = option(TKG_OPT_INJECT_STALL);
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.gridDim = dim3(p.num_tiles * SPLIT, 1, 1);
+  int nattr = 0;
+  if (SPLIT > 1) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = SPLIT;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p) != cudaSuccess) {
+    cudaGetLastError();
+    return TKG_ERR_CUDA;
+  }
+  return TKG_OK;
+}
+
+// K split for problems with few 128 x 128 output tiles: 2 or 3 CTAs per tile
+// when that still fits one wave, 0 to use the persistent kernel.  Every CTA's
+// stretch of K (ceil(stages / split) stages) must be non-empty.
+inline int choose_split(const Problem& pr, int stage_k) {
+  const int forced = option(TKG_OPT_SPLIT_K);
+  if (forced == 1) return 0;
+  int sms = 0;
+  if (device_sm_count(&sms) != TKG_OK) return 0;
+  const int tiles = ceil_div(pr.m, 128) * ceil_div(pr.n, 128);
+  const int stages = ceil_div(pr.k, stage_k);
+  int split = forced >= 2 ? forced : (tiles * 2 <= sms ? (sms / tiles < 3 ? sms / tiles : 3) : 0);
+  while (split >= 2 && (split - 1) * ceil_div(stages, split) >= stages) --split;
+  return split >= 2 ? split : 0;
 }
 
 // Cluster launch control unless TKG_OPT_SCHEDULER asks for the static schedule.

@@ -139,6 +139,15 @@ __device__ __forceinline__ bool clc_read(uint32_t resp, uint32_t& first_ctaid_x)
   return ok != 0;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the next kernel in the stream start launching its CTAs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the kernels this one depends on have completed and their memory
+// is visible (a no-op when launched without the programmatic attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- cluster barrier
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -12,11 +12,11 @@
 namespace tkg {
 
 // ------------------------------------------------------------------ options
-static std::atomic<int> g_opts[8];
+static std::atomic<int> g_opts[16];
 
 int option(tkg_option o) {
   const int i = int(o);
-  return (i > 0 && i < 8) ? g_opts[i].load(std::memory_order_relaxed) : 0;
+  return (i > 0 && i < 16) ? g_opts[i].load(std::memory_order_relaxed) : 0;
 }
 
 // ------------------------------------------------------------------ per-device state
@@ -76,31 +76,71 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-tkg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
-                     uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+// Encoding a tensor map costs about a microsecond, and a GEMM needs up to
+// five; small GEMMs are bound by that host work.  Each thread keeps the maps it
+// encoded in a small direct-mapped cache keyed by every encoding argument (a
+// map holds only the address and geometry, never the data).
+namespace {
+struct MapKey {
+  uint32_t dtype, rank, swizzle;
+  const void* base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  bool operator==(const MapKey& o) const {
+    return dtype == o.dtype && rank == o.rank && swizzle == o.swizzle && base == o.base && dims[0] == o.dims[0] &&
+           dims[1] == o.dims[1] && dims[2] == o.dims[2] && strides[0] == o.strides[0] &&
+           strides[1] == o.strides[1] && box[0] == o.box[0] && box[1] == o.box[1] && box[2] == o.box[2];
+  }
+};
+struct MapEntry {
+  bool valid = false;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSize = 64;
+thread_local MapEntry t_map_cache[kMapCacheSize];
+
+uint32_t key_hash(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  for (int i = 0; i < 3; ++i) h ^= (k.dims[i] + 0x7F4A7C15ull * (i + 1)) * 0xBF58476D1CE4E5B9ull;
+  h ^= (uint64_t(k.box[0]) << 32 | k.box[1]) * 0x94D049BB133111EBull;
+  h ^= uint64_t(k.dtype) << 40 ^ uint64_t(k.swizzle) << 48 ^ k.strides[0];
+  return uint32_t(h >> 32) % kMapCacheSize;
+}
+
+tkg_status encode_cached(CUtensorMap* map, const MapKey& key) {
+  MapEntry& e = t_map_cache[key_hash(key)];
+  if (e.valid && e.key == key) {
+    *map = e.map;
+    return TKG_OK;
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return TKG_ERR_CUDA;
-  const cuuint64_t dims[2] = {dim0, dim1};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CUtensorMapDataType(key.dtype), key.rank, const_cast<void*>(key.base), key.dims, key.strides,
+                  key.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CUtensorMapSwizzle(key.swizzle),
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TKG_ERR_INVALID_ARG;
+  e.valid = true;
+  e.key = key;
+  e.map = *map;
+  return TKG_OK;
+}
+}  // namespace
+
+tkg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                     uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+  MapKey k{uint32_t(dtype), 2u, uint32_t(swz), base, {dim0, dim1, 0}, {row_bytes, 0}, {box0, box1, 0}};
+  return encode_cached(map, k);
 }
 
 tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
                      uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                      uint32_t box2) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return TKG_ERR_CUDA;
-  const cuuint64_t dims[3] = {dim0, dim1, dim2};
-  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-  const cuuint32_t box[3] = {box0, box1, box2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? TKG_OK : TKG_ERR_INVALID_ARG;
+  MapKey k{uint32_t(dtype), 3u, uint32_t(CU_TENSOR_MAP_SWIZZLE_NONE), base, {dim0, dim1, dim2},
+           {stride1_bytes, stride2_bytes}, {box0, box1, box2}};
+  return encode_cached(map, k);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -201,7 +241,7 @@ size_t tkg_scale_bytes(int rows, int k, int block) {
 
 tkg_status tkg_set_option(tkg_option o, int value) {
   const int i = int(o);
-  if (i <= 0 || i >= 8 || value < 0) return TKG_ERR_INVALID_ARG;
+  if (i <= 0 || i > int(TKG_OPT_SPLIT_K) || value < 0) return TKG_ERR_INVALID_ARG;
   if (o == TKG_OPT_CTA_GROUP && value > 2) return TKG_ERR_INVALID_ARG;
   g_opts[i].store(value, std::memory_order_relaxed);
   return TKG_OK;

@@ -157,9 +157,11 @@ typedef enum {
                                   (test of the timeout path; output is garbage) */
   TKG_OPT_MAX_CLUSTERS = 5,   /* cap on persistent clusters (0: fill the GPU) */
   TKG_OPT_ACC_STAGES = 6,     /* BF16 only: 1 = single accumulator buffer (0: double) */
-  TKG_OPT_SCHEDULER = 7       /* 0: cluster launch control (one cluster per tile, running
+  TKG_OPT_SCHEDULER = 7,      /* 0: cluster launch control (one cluster per tile, running
                                   clusters take over pending ones); 1: static persistent
                                   grid (TKG_OPT_MAX_CLUSTERS applies only here) */
+  TKG_OPT_SPLIT_K = 8         /* 0: split K across 2-3 CTAs when the output has few 128x128
+                                  tiles (skinny M); 1: never; 2, 3: that split whenever valid */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);

@@ -16,7 +16,7 @@ FMTS = ["bf16", "mxfp8", "nvfp4"]
 
 
 ALL_OPTIONS = (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
-               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER)
+               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER, tkg.OPT_SPLIT_K)
 
 
 @pytest.fixture(autouse=True)
@@ -28,8 +28,9 @@ def _reset_options():
         tkg.set_option(o, 0)
 
 
-def _check(fmt, m, n, k, seed, alpha=1.0, cta_group=0):
+def _check(fmt, m, n, k, seed, alpha=1.0, cta_group=0, split=0):
     tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    tkg.set_option(tkg.OPT_SPLIT_K, split)
     ops = Operands(fmt, m, n, k, seed, alpha)
     D = run_gemm(fmt, ops.upload(), m, n, k, alpha)
     assert tkg.device_status() == tkg.OK
@@ -46,8 +47,21 @@ SHAPES = [(512, 512, 512), (300, 264, 320), (129, 136, 96), (1, 8, 32), (257, 52
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("shape", SHAPES)
 def test_gemm_matches_oracle(fmt, shape, cta_group):
+    # persistent kernel (split-K disabled)
     m, n, k = shape
-    _check(fmt, m, n, k, seed=1000 + m + n + k, alpha=1.0, cta_group=cta_group)
+    _check(fmt, m, n, k, seed=1000 + m + n + k, alpha=1.0, cta_group=cta_group, split=1)
+
+
+SPLIT_SHAPES = [(512, 512, 512), (300, 264, 320), (16, 1024, 2048), (5, 136, 4000), (128, 256, 96)]
+
+
+@pytest.mark.parametrize("split", [0, 2, 3])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", SPLIT_SHAPES)
+def test_split_k_matches_oracle(fmt, shape, split):
+    # split-K kernel: automatic choice, or forced to 2 / 3 CTAs per tile
+    m, n, k = shape
+    _check(fmt, m, n, k, seed=2000 + m + n + k, alpha=0.5, split=split)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -185,11 +199,13 @@ def test_every_code_pair_exact(fmt, cta_group):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_scale_index_exact(fmt, cta_group):
+@pytest.mark.parametrize("cta_group,split", [(1, 1), (2, 1), (0, 3)])
+def test_scale_index_exact(fmt, cta_group, split):
     # one nonzero block per row; distinct scale codes per (row, block); rows
-    # cross 128-row tiles and the CTA pair, blocks cross stages and atoms
+    # cross 128-row tiles and the CTA pair, blocks cross stages, atoms and the
+    # K stretches of a split-K cluster
     tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    tkg.set_option(tkg.OPT_SPLIT_K, split)
     bs = oracle.BLOCK[fmt]
     m, n, k = 520, 264, 1536
     kb = k // bs

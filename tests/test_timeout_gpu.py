@@ -14,12 +14,13 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_stalled_wait_times_out_and_recovers(fmt, cta_group):
+@pytest.mark.parametrize("cta_group,split", [(1, 1), (2, 1), (0, 2)])
+def test_stalled_wait_times_out_and_recovers(fmt, cta_group, split):
     m, n, k = 512, 512, 1024
     ops = Operands(fmt, m, n, k, seed=77)
     dev = ops.upload()
     tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    tkg.set_option(tkg.OPT_SPLIT_K, split)
     try:
         tkg.set_option(tkg.OPT_TIMEOUT_MS, 100)
         tkg.set_option(tkg.OPT_INJECT_STALL, 1)
@@ -38,4 +39,5 @@ def test_stalled_wait_times_out_and_recovers(fmt, cta_group):
     ref, S = ops.reference()
     assert_within_tolerance(bf16_to_f64(D), ref, S, "after recovery")
     tkg.set_option(tkg.OPT_CTA_GROUP, 0)
+    tkg.set_option(tkg.OPT_SPLIT_K, 0)
     torch.cuda.synchronize()
