@@ -52,6 +52,7 @@ struct GemmParams {
   unsigned int* status;      // device status word (error bits)
   unsigned long long timeout_ns;
   int inject_stall;          // test hook: the MMA role waits on a barrier nothing arrives on
+  int raster_group;          // M-blocks per raster band (see tile_coords)
 };
 
 template <int FMT>
@@ -96,15 +97,16 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
   return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t(128 >> 4) << 32) | (1ull << 46);
 }
 
-// Tile order: bands of kRasterGroup M-blocks walked N-fastest-within-band, so the
-// clusters running together share A rows and B columns in L2.
-constexpr int kRasterGroup = 8;
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  const int group_size = kRasterGroup * tiles_n;
-  const int group = t / group_size;
-  const int first_m = group * kRasterGroup;
-  const int gm = min(tiles_m - first_m, kRasterGroup);
-  const int r = t - group * group_size;
+// Tile order: bands of `group` M-blocks walked N-fastest-within-band, so the
+// clusters running together share A rows and B columns in L2, and a band's A
+// panels stay in L2 while B streams past (the host sizes the band from the L2
+// capacity and the panel size).
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group, int& mb, int& nb) {
+  const int group_size = group * tiles_n;
+  const int band = t / group_size;
+  const int first_m = band * group;
+  const int gm = min(tiles_m - first_m, group);
+  const int r = t - band * group_size;
   mb = first_m + r % gm;
   nb = r / gm;
 }
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll 1
       for (int t = cluster_id; t >= 0 && ok;) {
         int mb, nb;
-        tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+        tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
         const int a_row = mb * C::kMmaM + int(rank) * C::kCtaM;
         const int b_row = nb * BN + int(rank) * C::kBRows;
         const int sfb_block0 = (nb * BN) / 128;
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll 1
     for (int t = cluster_id; t >= 0;) {
       int mb, nb;
-      tile_coords(t, p.tiles_m, p.tiles_n, mb, nb);
+      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
       uint32_t ok = 0;
       if (lane == 0) ok = wait_bar<false>(accf_bar(acc), accph, ctl) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, ok, 0);

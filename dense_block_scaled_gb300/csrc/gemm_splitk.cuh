@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(384, 1)
   ctl.timeout_ns = p.timeout_ns;
 
   int mb, nb;
-  tile_coords(int(blockIdx.x) / SPLIT, p.tiles_m, p.tiles_n, mb, nb);
+  tile_coords(int(blockIdx.x) / SPLIT, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
   // this CTA's stretch of K (in stages); the host keeps every stretch non-empty
   const int per = (p.num_kstages + SPLIT - 1) / SPLIT;
   const int ks0 = int(rank) * per;

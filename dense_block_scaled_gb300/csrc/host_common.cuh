@@ -30,6 +30,25 @@ struct Problem {
 int option(tkg_option o);
 tkg_status device_status_word(unsigned int** out);   // lazily allocated per device
 tkg_status device_sm_count(int* out);
+tkg_status device_l2_bytes(int* out);
+
+// M-blocks per raster band: as many as let the band's A panels (rows x K
+// bytes each) fill about a quarter of L2, between 4 and 32 (measured best at
+// 16384^3 on GB300: BF16 4-8, MXFP8 8, NVFP4 16 bands; at half of L2 NVFP4
+// loses 9%).
+inline int raster_group(int block_rows, int k, int fmt, int tiles_m) {
+  const int forced = option(TKG_OPT_RASTER_GROUP);
+  if (forced > 0) return forced < tiles_m ? forced : (tiles_m > 0 ? tiles_m : 1);
+  int l2 = 0;
+  if (device_l2_bytes(&l2) != TKG_OK || l2 <= 0) l2 = 96 << 20;
+  const double bytes_per_elem = fmt == 0 ? 2.0 : (fmt == 1 ? 1.0 : 0.5);
+  const double panel = double(block_rows) * double(k) * bytes_per_elem;
+  int g = int(0.25 * double(l2) / (panel > 1.0 ? panel : 1.0) + 0.5);
+  if (g < 4) g = 4;
+  if (g > 32) g = 32;
+  if (g > tiles_m) g = tiles_m > 0 ? tiles_m : 1;
+  return g;
+}
 
 // ---- tensor maps (tkg_api.cu)
 tkg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
@@ -106,6 +125,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
+  p.raster_group = raster_group(C::kMmaM, pr.k, FMT, p.tiles_m);
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;
@@ -217,6 +237,7 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
+  p.raster_group = raster_group(C::BM, pr.k, FMT, p.tiles_m);
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

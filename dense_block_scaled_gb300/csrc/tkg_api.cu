@@ -23,6 +23,7 @@ int option(tkg_option o) {
 static std::mutex g_dev_mu;
 static unsigned int* g_status[64] = {};
 static int g_sms[64] = {};
+static int g_l2[64] = {};
 
 static int current_device() {
   int dev = -1;
@@ -54,6 +55,18 @@ tkg_status device_sm_count(int* out) {
     g_sms[dev] = n;
   }
   *out = g_sms[dev];
+  return TKG_OK;
+}
+
+tkg_status device_l2_bytes(int* out) {
+  const int dev = current_device();
+  if (dev < 0) return TKG_ERR_CUDA;
+  if (g_l2[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return TKG_ERR_CUDA;
+    g_l2[dev] = n;
+  }
+  *out = g_l2[dev];
   return TKG_OK;
 }
 
@@ -241,7 +254,7 @@ size_t tkg_scale_bytes(int rows, int k, int block) {
 
 tkg_status tkg_set_option(tkg_option o, int value) {
   const int i = int(o);
-  if (i <= 0 || i > int(TKG_OPT_SPLIT_K) || value < 0) return TKG_ERR_INVALID_ARG;
+  if (i <= 0 || i > int(TKG_OPT_RASTER_GROUP) || value < 0) return TKG_ERR_INVALID_ARG;
   if (o == TKG_OPT_CTA_GROUP && value > 2) return TKG_ERR_INVALID_ARG;
   g_opts[i].store(value, std::memory_order_relaxed);
   return TKG_OK;

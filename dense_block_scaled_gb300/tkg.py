@@ -21,6 +21,7 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = ran
 OPT_CTA_GROUP, OPT_SINGLE_STAGE, OPT_TIMEOUT_MS, OPT_INJECT_STALL, OPT_MAX_CLUSTERS, OPT_ACC_STAGES = 1, 2, 3, 4, 5, 6
 OPT_SCHEDULER = 7
 OPT_SPLIT_K = 8
+OPT_RASTER_GROUP = 9
 
 EXPORTS = [
     "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",

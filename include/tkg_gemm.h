@@ -160,8 +160,9 @@ typedef enum {
   TKG_OPT_SCHEDULER = 7,      /* 0: cluster launch control (one cluster per tile, running
                                   clusters take over pending ones); 1: static persistent
                                   grid (TKG_OPT_MAX_CLUSTERS applies only here) */
-  TKG_OPT_SPLIT_K = 8         /* 0: split K across 2-3 CTAs when the output has few 128x128
+  TKG_OPT_SPLIT_K = 8,        /* 0: split K across 2-3 CTAs when the output has few 128x128
                                   tiles (skinny M); 1: never; 2, 3: that split whenever valid */
+  TKG_OPT_RASTER_GROUP = 9    /* M-blocks per tile-order band (0: sized from L2 and K) */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);

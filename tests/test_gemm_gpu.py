@@ -16,7 +16,8 @@ FMTS = ["bf16", "mxfp8", "nvfp4"]
 
 
 ALL_OPTIONS = (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
-               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER, tkg.OPT_SPLIT_K)
+               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER, tkg.OPT_SPLIT_K,
+               tkg.OPT_RASTER_GROUP)
 
 
 @pytest.fixture(autouse=True)
