@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--skinny", default="16,128,1024", help="M values of the skinny N=K=8192 GEMMs reported")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-quant", action="store_true", help="skip the quantiser timings")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
     return ap.parse_args()
 
@@ -138,7 +139,7 @@ class ClockSampler:
 class Workload:
     """One GEMM (format, M=N=K=size) resident in HBM in `groups` identical copies."""
 
-    def __init__(self, fmt, size, seed, l2_bytes, torch, tkg, synth, keep_host=False, mnk=None):
+    def __init__(self, fmt, size, seed, l2_bytes, torch, tkg, synth, keep_host=False, mnk=None, keep_fp32=False):
         self.fmt, self.size = fmt, size
         self.m, self.n, self.k = mnk if mnk else (size, size, size)
         m, n, k = self.m, self.n, self.k
@@ -146,6 +147,7 @@ class Workload:
         a, b = synth.gemm_inputs_f32(m, n, k, seed)
         dev = torch.device("cuda")
         self.host = None
+        self.fp32 = None
         if fmt == "bf16":
             ca, cb = synth.bf16_codes(a), synth.bf16_codes(b)
             del a, b
@@ -174,6 +176,8 @@ class Workload:
                 tkg.quantize_nvfp4(X, QA, SA, TA)
                 tkg.quantize_nvfp4(Y, QB, SB, TB)
                 ops = [QA, QB, SA, SB, TA, TB]
+            if keep_fp32:
+                self.fp32 = X
             del X, Y
             torch.cuda.synchronize()
         self.in_bytes = sum(int(o.numel() * o.element_size()) for o in ops if o is not None)
@@ -233,6 +237,38 @@ def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flu
     if st != tkg.OK:
         raise RuntimeError(f"device status after timing: {tkg.status_string(st)}")
     return ms / 1e3 / steps
+
+
+def quant_timings(X, steps, warmup, torch, tkg, hbm_gbs):
+    """Device time of the library's quantisers on one FP32 operand (rows x k,
+    larger than L2, so no flush is needed between launches).  Algorithmic bytes
+    per element: MXFP8 reads 4 and writes 1 + 1/32 (codes, scales); NVFP4 makes
+    two passes, the tensor amax (4 read) and the quantisation (4 read, 1/2 + 1/16
+    written)."""
+    rows, k = X.shape
+    dev = X.device
+    out = {}
+    for fmt, bs, cols, bpe in (("mxfp8", 32, k, 4 + 1 + 1 / 32), ("nvfp4", 16, k // 2, 8 + 0.5 + 1 / 16)):
+        Q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        S = torch.empty((tkg.scale_bytes(rows, k, bs),), dtype=torch.uint8, device=dev)
+        T = torch.empty(1, dtype=torch.float32, device=dev)
+        run = (lambda: tkg.quantize_mxfp8(X, Q, S)) if fmt == "mxfp8" else (lambda: tkg.quantize_nvfp4(X, Q, S, T))
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        gbs = rows * k * bpe / t / 1e9
+        out[fmt] = {"us": t * 1e6, "gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "bytes_per_elem": bpe,
+                    "shape": [rows, k]}
+        del Q, S, T
+    return out
 
 
 def graph_seconds(w, steps, torch, tkg):
@@ -402,16 +438,19 @@ def run_ours(args):
                 "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
                 "measured_peak_tflops": peak_meas, "input_groups": w.groups}
 
-    by_format, sweep, skinny = {}, {}, {}
+    by_format, sweep, skinny, quant = {}, {}, {}, {}
     e2e = None
     if rank == 0:
         by_format[hf] = fmt_entry(head, t_head)
         for fmt in formats:
             if fmt == hf:
                 continue
-            w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth)
+            w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth,
+                         keep_fp32=(fmt != "bf16" and not args.no_quant and not quant))
             by_format[fmt] = fmt_entry(w, time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2,
                                                           flush_buf))
+            if w.fp32 is not None:
+                quant = quant_timings(w.fp32, 20, 3, torch, tkg, pk["hbm_gbs"])
             del w
             torch.cuda.empty_cache()
         for s in [int(x) for x in args.sweep.split(",") if x]:
@@ -471,6 +510,7 @@ def run_ours(args):
             "formats": by_format,
             "sweep_bf16": sweep,
             "skinny": skinny,
+            "quantize": quant,
             "kernel_hash": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

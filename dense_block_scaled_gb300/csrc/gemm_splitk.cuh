@@ -234,7 +234,10 @@ __global__ void __launch_bounds__(384, 1)
   const int row = q * 32 + lane;       // tile row this thread holds
   uint32_t v[2][32];
   uint32_t have = 0;
-  if (epi) {
+  // a quadrant whose 32 rows all lie beyond M (M = 16 leaves three of four
+  // idle) has nothing to reduce or store
+  const bool live = mb * C::BM + q * 32 < p.m;
+  if (epi && live) {
     if (lane == 0) have = wait_bar<false>(accf_bar, 0u, ctl) ? 1u : 0u;
     have = __shfl_sync(0xffffffffu, have, 0);
     if (have) {

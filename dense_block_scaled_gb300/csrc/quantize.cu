@@ -1,6 +1,6 @@
 // quantize.cu -- FP32 -> MXFP8 / NVFP4 quantisers and the row-major -> tiled
-// scale-layout conversion.  All HBM-bound: coalesced 16-byte loads, grid sized
-// to a multiple of the SM count, grid-stride loops.
+// scale-layout conversion.  All HBM-bound: coalesced 16-byte loads, several in
+// flight per thread, one wave of resident blocks, grid-stride loops.
 //
 // Quantisation rules are those of the workload definition (MXFP8: E8M0 scale
 // 2^ceil(log2(amax/448)) per 1x32 block, E4M3 RNE saturating; NVFP4: FP32
@@ -56,7 +56,16 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// One warp = four 32-element blocks per pass; lane l takes 4 consecutive elements.
+// Work layout shared by both quantisers: a warp pass covers 512 contiguous
+// bytes of X (lane l loads the float4 at 16*l), i.e. four 32-element MXFP8
+// blocks or eight 16-element NVFP4 blocks.  Each warp takes kUnroll
+// consecutive passes per loop trip and issues all their loads before any
+// arithmetic, so that every SM keeps enough bytes in flight to cover the HBM
+// latency.  When k/bs is a multiple of 4, the four scale bytes of blocks
+// kb..kb+3 (kb % 4 == 0) of a row are adjacent in the tiled layout and go out
+// as one 32-bit store.
+constexpr int kUnroll = 4;
+
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kblk, const float* __restrict__ X,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
                                                           int ka) {
@@ -64,24 +73,40 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kb
   const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const long long passes = (nblk + 3) / 4;
-  for (long long w = warp0; w < passes; w += nwarps) {
-    const long long b = w * 4 + (lane >> 3);
-    const bool valid = b < nblk;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) x = __ldcs(reinterpret_cast<const float4*>(X + b * 32 + 4 * (lane & 7)));
-    float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    const int e = mx_exponent(a);
-    const float inv = __uint_as_float(uint32_t(127 - e) << 23);   // 2^-e, a normal float for e in [-127, 120]
-    if (valid) {
-      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x.x, inv), __fmul_rn(x.y, inv));
-      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x.z, inv), __fmul_rn(x.w, inv));
-      *reinterpret_cast<uint32_t*>(Q + b * 32 + 4 * (lane & 7)) = lo | (hi << 16);
-      if ((lane & 7) == 0) {
+  const bool packed_sf = (kblk & 3) == 0;
+  for (long long w = warp0 * kUnroll; w < passes; w += nwarps * kUnroll) {
+    float4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long b = (w + u) * 4 + (lane >> 3);
+      x[u] = b < nblk ? __ldcs(reinterpret_cast<const float4*>(X + b * 32 + 4 * (lane & 7)))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long b = (w + u) * 4 + (lane >> 3);
+      float a = fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w)));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+      const int e = mx_exponent(a);
+      const float inv = __uint_as_float(uint32_t(127 - e) << 23);   // 2^-e, a normal float for e in [-127, 120]
+      const uint32_t code = uint32_t(e + 127);
+      // scale bytes of the pass's four blocks, gathered in lane 0
+      const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 8);
+      const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 16);
+      const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 24);
+      if (b < nblk) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[u].x, inv), __fmul_rn(x[u].y, inv));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[u].z, inv), __fmul_rn(x[u].w, inv));
+        *reinterpret_cast<uint32_t*>(Q + b * 32 + 4 * (lane & 7)) = lo | (hi << 16);
         const int r = int(b / kblk), kb = int(b % kblk);
-        SF[sf_tiled_offset(r, kb, ka)] = uint8_t(e + 127);
+        if (packed_sf) {
+          if (lane == 0)
+            *reinterpret_cast<uint32_t*>(SF + sf_tiled_offset(r, kb, ka)) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+        } else if ((lane & 7) == 0) {
+          SF[sf_tiled_offset(r, kb, ka)] = uint8_t(code);
+        }
       }
     }
   }
@@ -92,9 +117,16 @@ __global__ void __launch_bounds__(256) amax_kernel(long long n4, const float* __
                                                    unsigned int* __restrict__ out) {
   float a = 0.f;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(X) + i);
-    a = fmaxf(a, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+  for (long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i0 < n4; i0 += stride * kUnroll) {
+    float4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      x[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(X) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      a = fmaxf(a, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
   }
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   __shared__ float red[8];
@@ -113,7 +145,6 @@ __global__ void tensor_scale_kernel(unsigned int* __restrict__ word) {
   *reinterpret_cast<float*>(word) = __fdiv_rn(amax, 2688.0f);
 }
 
-// One warp = eight 16-element blocks per pass; lane l takes 4 consecutive elements.
 __global__ void __launch_bounds__(256) quant_nvfp4_kernel(long long nblk, int kblk, const float* __restrict__ X,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF, int ka,
                                                           const float* __restrict__ tptr) {
@@ -121,33 +152,48 @@ __global__ void __launch_bounds__(256) quant_nvfp4_kernel(long long nblk, int kb
   const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const long long passes = (nblk + 7) / 8;
+  const bool packed_sf = (kblk & 3) == 0;
   const float t = __ldg(tptr);
   const float d = __fmul_rn(6.0f, t);
-  for (long long w = warp0; w < passes; w += nwarps) {
-    const long long b = w * 8 + (lane >> 2);
-    const bool valid = b < nblk;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) x = __ldcs(reinterpret_cast<const float4*>(X + b * 16 + 4 * (lane & 3)));
-    float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    uint32_t s = 0;
-    float den = 0.f;
-    if (t > 0.f) {
-      s = cvt_e4m3x2(__fdiv_rn(a, d), 0.f) & 0xFFu;
-      den = __fmul_rn(e4m3_value(s), t);
+  for (long long w = warp0 * kUnroll; w < passes; w += nwarps * kUnroll) {
+    float4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long b = (w + u) * 8 + (lane >> 2);
+      x[u] = b < nblk ? __ldcs(reinterpret_cast<const float4*>(X + b * 16 + 4 * (lane & 3)))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (valid) {
-      uint32_t packed = 0;
-      if (den > 0.f) {
-        const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x.x, den), __fdiv_rn(x.y, den));
-        const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x.z, den), __fdiv_rn(x.w, den));
-        packed = lo | (hi << 8);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long b = (w + u) * 8 + (lane >> 2);
+      float a = fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w)));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      uint32_t s = 0;
+      float den = 0.f;
+      if (t > 0.f) {
+        s = cvt_e4m3x2(__fdiv_rn(a, d), 0.f) & 0xFFu;
+        den = __fmul_rn(e4m3_value(s), t);
       }
-      *reinterpret_cast<uint16_t*>(Q + b * 8 + 2 * (lane & 3)) = uint16_t(packed);
-      if ((lane & 3) == 0) {
+      // scale bytes of blocks j..j+3 gathered in lanes 0 and 16
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 4);
+      const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 8);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 12);
+      if (b < nblk) {
+        uint32_t packed = 0;
+        if (den > 0.f) {
+          const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x[u].x, den), __fdiv_rn(x[u].y, den));
+          const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x[u].z, den), __fdiv_rn(x[u].w, den));
+          packed = lo | (hi << 8);
+        }
+        *reinterpret_cast<uint16_t*>(Q + b * 8 + 2 * (lane & 3)) = uint16_t(packed);
         const int r = int(b / kblk), kb = int(b % kblk);
-        SF[sf_tiled_offset(r, kb, ka)] = uint8_t(s);
+        if (packed_sf) {
+          if ((lane & 15) == 0)
+            *reinterpret_cast<uint32_t*>(SF + sf_tiled_offset(r, kb, ka)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        } else if ((lane & 3) == 0) {
+          SF[sf_tiled_offset(r, kb, ka)] = uint8_t(s);
+        }
       }
     }
   }
@@ -163,11 +209,19 @@ __global__ void __launch_bounds__(256) scales_to_tiled_kernel(int rows, int kblo
   }
 }
 
-static int grid_for(long long work_items, int per_block) {
+// Blocks for `work_items` threads of `per_block`, capped at one full wave of
+// resident blocks (the kernels loop over the rest).
+template <typename Kern>
+static int grid_for(Kern kern, long long work_items, int per_block) {
   int sms = 148;
   device_sm_count(&sms);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, per_block, 0) != cudaSuccess || per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 4;
+  }
   long long want = (work_items + per_block - 1) / per_block;
-  long long cap = (long long)sms * 8;
+  long long cap = (long long)sms * per_sm;
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   return int(want);
@@ -189,7 +243,8 @@ tkg_status tkg_quantize_mxfp8(int rows, int k, const float* X, void* Q, void* sf
   const int kblk = k / 32, ka = (kblk + 3) / 4;
   if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 32), stream) != cudaSuccess) return TKG_ERR_CUDA;
   const long long nblk = (long long)rows * kblk;
-  quant_mxfp8_kernel<<<grid_for((nblk + 3) / 4 * 32, 256), 256, 0, stream>>>(
+  const int grid = grid_for(quant_mxfp8_kernel, ((nblk + 3) / 4 + kUnroll - 1) / kUnroll * 32, 256);
+  quant_mxfp8_kernel<<<grid, 256, 0, stream>>>(
       nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
 }
@@ -207,10 +262,11 @@ tkg_status tkg_quantize_nvfp4(int rows, int k, const float* X, void* Q, void* sf
   if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 16), stream) != cudaSuccess) return TKG_ERR_CUDA;
   unsigned int* word = reinterpret_cast<unsigned int*>(tensor_scale);
   const long long n4 = (long long)rows * k / 4;
-  amax_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(n4, X, word);
+  amax_kernel<<<grid_for(amax_kernel, (n4 + kUnroll - 1) / kUnroll, 256), 256, 0, stream>>>(n4, X, word);
   tensor_scale_kernel<<<1, 1, 0, stream>>>(word);
   const long long nblk = (long long)rows * kblk;
-  quant_nvfp4_kernel<<<grid_for((nblk + 7) / 8 * 32, 256), 256, 0, stream>>>(
+  const int grid = grid_for(quant_nvfp4_kernel, ((nblk + 7) / 8 + kUnroll - 1) / kUnroll * 32, 256);
+  quant_nvfp4_kernel<<<grid, 256, 0, stream>>>(
       nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka, tensor_scale);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
 }
@@ -223,8 +279,8 @@ tkg_status tkg_scales_to_tiled(int rows, int kblocks, const void* src, int ld, v
   const size_t bytes = size_t((rows + 127) / 128) * 128 * size_t(ka) * 4;
   if (cudaMemsetAsync(dst, 0, bytes, stream) != cudaSuccess) return TKG_ERR_CUDA;
   const long long n = (long long)rows * kblocks;
-  scales_to_tiled_kernel<<<grid_for(n, 256), 256, 0, stream>>>(rows, kblocks, static_cast<const uint8_t*>(src), ld,
-                                                               static_cast<uint8_t*>(dst), ka);
+  scales_to_tiled_kernel<<<grid_for(scales_to_tiled_kernel, n, 256), 256, 0, stream>>>(
+      rows, kblocks, static_cast<const uint8_t*>(src), ld, static_cast<uint8_t*>(dst), ka);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
 }
 

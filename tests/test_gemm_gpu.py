@@ -53,7 +53,7 @@ def test_gemm_matches_oracle(fmt, shape, cta_group):
     _check(fmt, m, n, k, seed=1000 + m + n + k, alpha=1.0, cta_group=cta_group, split=1)
 
 
-SPLIT_SHAPES = [(512, 512, 512), (300, 264, 320), (16, 1024, 2048), (5, 136, 4000), (128, 256, 96)]
+SPLIT_SHAPES = [(512, 512, 512), (300, 264, 320), (16, 1024, 2048), (5, 136, 4000), (128, 256, 96), (33, 256, 512)]
 
 
 @pytest.mark.parametrize("split", [0, 2, 3])

@@ -10,7 +10,9 @@ from helpers import tiled_scales, to_dev
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(1, 32), (130, 96), (257, 4000), (1024, 2048)]
+# k/bs both a multiple of 4 (packed scale stores) and not; sizes spanning
+# several grid-stride trips with a ragged last one
+SHAPES = [(1, 32), (130, 96), (257, 4000), (1024, 2048), (333, 2080), (4099, 8192)]
 
 
 @pytest.mark.parametrize("rows,k", SHAPES)
