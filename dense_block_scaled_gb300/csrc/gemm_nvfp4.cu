@@ -11,6 +11,11 @@ tkg_status launch_nvfp4(const Problem& pr, cudaStream_t s) {
   const int cg = option(TKG_OPT_CTA_GROUP);
   // few output tiles (skinny M): split K across a cluster
   const int split = choose_split(pr, FmtTraits<FMT_NVFP4>::kStageK);
+  if (split >= 2 && pr.m <= 32) {
+    // short A tiles leave room for a deeper B pipeline
+    if (split == 2) return launch_splitk<FMT_NVFP4, 2, 8, 32>(pr, s);
+    return launch_splitk<FMT_NVFP4, 3, 8, 32>(pr, s);
+  }
   if (split == 2) return launch_splitk<FMT_NVFP4, 2, 5>(pr, s);
   if (split == 3) return launch_splitk<FMT_NVFP4, 3, 5>(pr, s);
   if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_NVFP4, 2, 256, 1, 1>(pr, s);

@@ -11,12 +11,30 @@
 //
 // Same operand formats, layouts, roles and bounded waits as gemm_kernel.cuh;
 // single-CTA MMAs (M = 128, N = 128) and one tile per cluster.
+//
+// For M <= 32 the A tile is loaded AROWS = 32 rows high: the MMA still reads
+// 128 rows, but rows 32..127 of its accumulator are never stored, so whatever
+// shared memory it reads there does not matter, and the freed 12 KB per stage
+// buys a deeper pipeline for the B stream.
+//
+// The partials move with st.async, which counts its bytes on an mbarrier in
+// the leader; the leader tells the others that its stage buffers are free by a
+// relaxed remote arrive.  No cluster-wide barrier sits on the path.
 #pragma once
 #include "gemm_kernel.cuh"
 
 namespace tkg {
 
-template <int FMT, int SPLIT, int STAGES>
+// 16-byte store into another CTA's shared memory that completes `bytes` of
+// transaction count on an mbarrier there.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+               : "memory");
+}
+
+template <int FMT, int SPLIT, int STAGES, int AROWS = 128>
 struct SplitKConfig {
   using T = FmtTraits<FMT>;
   static constexpr bool kScaled = FMT != FMT_BF16;
@@ -25,7 +43,7 @@ struct SplitKConfig {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
   static constexpr int kRowBytes = 128;
-  static constexpr int kABytes = BM * kRowBytes;
+  static constexpr int kABytes = AROWS * kRowBytes;   // rows loaded; the MMA reads BM
   static constexpr int kBBytes = BN * kRowBytes;
   static constexpr int kSfaBytes = T::kSfAtoms * 512;
   static constexpr int kSfbBytes = T::kSfAtoms * 512;   // one 128-row scale block
@@ -34,7 +52,7 @@ struct SplitKConfig {
   static constexpr int kEpiBufBytes = 32 * 64;
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kPartialBytes = BM * BN * 4;   // one CTA's FP32 accumulator
-  static constexpr int kNumBars = 2 * STAGES + 3;
+  static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kTxBytes = uint32_t(kABytes + kBBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
@@ -44,6 +62,9 @@ struct SplitKConfig {
   static constexpr int kRegions = (512 - BN) / kRegionCols;
   static constexpr int kTmemCols = 512;
   static_assert(SPLIT >= 1 && SPLIT <= 4, "split factor");
+  static_assert(AROWS == 128 || AROWS == 32, "A tile height");
+  // the MMA's 128-row read of a short A tile stays inside its stage
+  static_assert(BM * kRowBytes <= kStageBytes, "A read past the stage");
   static_assert((SPLIT - 1) * kPartialBytes <= STAGES * kStageBytes, "partials must fit the stage buffers");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static constexpr uint32_t kIdesc =
@@ -51,12 +72,12 @@ struct SplitKConfig {
                       : idesc_bs(BM, BN, FMT == FMT_NVFP4 ? 1u : 0u, FMT == FMT_MXFP8 ? 1u : 0u, 0u, 0u);
 };
 
-template <int FMT, int SPLIT, int STAGES>
+template <int FMT, int SPLIT, int STAGES, int AROWS>
 __global__ void __launch_bounds__(384, 1)
     gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                        const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
-  using C = SplitKConfig<FMT, SPLIT, STAGES>;
+  using C = SplitKConfig<FMT, SPLIT, STAGES, AROWS>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
@@ -82,6 +103,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t accf_bar = bars + uint32_t(8 * (2 * STAGES));
   const uint32_t drain_bar = accf_bar + 8;
   const uint32_t never_bar = drain_bar + 8;
+  const uint32_t go_bar = never_bar + 8;     // others: the leader's stage buffers are free
+  const uint32_t part_bar = go_bar + 8;      // leader: all partial bytes have landed
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -92,6 +115,8 @@ __global__ void __launch_bounds__(384, 1)
     ptx::mbar_init(accf_bar, 1);
     ptx::mbar_init(drain_bar, 1);
     ptx::mbar_init(never_bar, 1);
+    ptx::mbar_init(go_bar, 1);
+    ptx::mbar_init(part_bar, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
@@ -255,38 +280,53 @@ __global__ void __launch_bounds__(384, 1)
 
   // ------------------------------------------------------------------ split-K reduction
   if constexpr (SPLIT > 1) {
-    // every CTA's MMAs are done, so the leader's stage buffers are free
-    ptx::tc_fence_before();
-    ptx::cluster_sync();
-    if (epi && !leader && have) {
-      const uint32_t dst = ptx::map_to_rank(base + uint32_t((rank - 1) * C::kPartialBytes), 0);
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t a = dst + uint32_t(row * 512) + uint32_t((((h * 16 + c * 8 + j) ^ row) & 31) * 16);
-          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v[c][4 * j]),
-                       "r"(v[c][4 * j + 1]), "r"(v[c][4 * j + 2]), "r"(v[c][4 * j + 3])
-                       : "memory");
-        }
-    }
-    ptx::cluster_sync();
-    if (epi && leader && have) {
+    // quadrants with rows below M; each of their warps moves 32 rows x 64 columns
+    const int rows_left = p.m - mb * C::BM;
+    const int live_q = rows_left >= C::BM ? 4 : (rows_left + 31) / 32;
+    const uint32_t part_bytes = uint32_t((SPLIT - 1) * live_q * 2) * uint32_t(32 * 64 * 4);
+    if (leader) {
+      if (warp == 4 && lane == 0 && have) {
+        // every MMA of this CTA has completed, so its stage buffers are free
+        ptx::mbar_arrive_expect_tx(part_bar, part_bytes);
 #pragma unroll 1
-      for (int r = 1; r < SPLIT; ++r) {
-        const uint32_t src = base + uint32_t((r - 1) * C::kPartialBytes);
+        for (uint32_t r = 1; r < uint32_t(SPLIT); ++r) ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(go_bar, r));
+      }
+      if (epi && have) {
+        uint32_t ok = 0;
+        if (lane == 0) ok = wait_bar<false>(part_bar, 0u, ctl) ? 1u : 0u;
+        have = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (epi && have) {
+#pragma unroll 1
+        for (int r = 1; r < SPLIT; ++r) {
+          const uint32_t src = base + uint32_t((r - 1) * C::kPartialBytes);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t w0, w1, w2, w3;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                           : "r"(partial_addr(src, h * 16 + c * 8 + j)));
+              v[c][4 * j] = __float_as_uint(__uint_as_float(v[c][4 * j]) + __uint_as_float(w0));
+              v[c][4 * j + 1] = __float_as_uint(__uint_as_float(v[c][4 * j + 1]) + __uint_as_float(w1));
+              v[c][4 * j + 2] = __float_as_uint(__uint_as_float(v[c][4 * j + 2]) + __uint_as_float(w2));
+              v[c][4 * j + 3] = __float_as_uint(__uint_as_float(v[c][4 * j + 3]) + __uint_as_float(w3));
+            }
+        }
+      }
+    } else if (epi && have) {
+      uint32_t ok = 0;
+      if (lane == 0) ok = wait_bar<false>(go_bar, 0u, ctl) ? 1u : 0u;
+      if (__shfl_sync(0xffffffffu, ok, 0)) {
+        const uint32_t dst = ptx::map_to_rank(base + uint32_t((rank - 1) * C::kPartialBytes), 0);
+        const uint32_t rbar = ptx::map_to_rank(part_bar, 0);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            uint32_t w0, w1, w2, w3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                         : "r"(partial_addr(src, h * 16 + c * 8 + j)));
-            v[c][4 * j] = __float_as_uint(__uint_as_float(v[c][4 * j]) + __uint_as_float(w0));
-            v[c][4 * j + 1] = __float_as_uint(__uint_as_float(v[c][4 * j + 1]) + __uint_as_float(w1));
-            v[c][4 * j + 2] = __float_as_uint(__uint_as_float(v[c][4 * j + 2]) + __uint_as_float(w2));
-            v[c][4 * j + 3] = __float_as_uint(__uint_as_float(v[c][4 * j + 3]) + __uint_as_float(w3));
+            const uint32_t a = dst + uint32_t(row * 512) + uint32_t((((h * 16 + c * 8 + j) ^ row) & 31) * 16);
+            st_async_v4(a, v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3], rbar);
           }
       }
     }

@@ -182,11 +182,11 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
 }
 
 // Split-K launch: one cluster of SPLIT CTAs per 128 x 128 output tile.
-template <int FMT, int SPLIT, int STAGES>
+template <int FMT, int SPLIT, int STAGES, int AROWS = 128>
 tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
-  using C = SplitKConfig<FMT, SPLIT, STAGES>;
+  using C = SplitKConfig<FMT, SPLIT, STAGES, AROWS>;
   using T = FmtTraits<FMT>;
-  auto kern = gemm_splitk_kernel<FMT, SPLIT, STAGES>;
+  auto kern = gemm_splitk_kernel<FMT, SPLIT, STAGES, AROWS>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TKG_ERR_CUDA;
   static bool attr_set[64] = {};
@@ -202,7 +202,7 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   const uint64_t row_bytes = FMT == FMT_BF16 ? uint64_t(pr.k) * 2 : kdim;
   const uint32_t boxk = bf16 ? 64 : 128;
   tkg_status st;
-  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::BM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, AROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::BN, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;

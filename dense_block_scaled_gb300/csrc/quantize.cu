@@ -1,13 +1,15 @@
 // quantize.cu -- FP32 -> MXFP8 / NVFP4 quantisers and the row-major -> tiled
-// scale-layout conversion.  All HBM-bound: coalesced 16-byte loads, several in
-// flight per thread, one wave of resident blocks, grid-stride loops.
+// scale-layout conversion.  All HBM-bound: 16-byte loads, several in flight per
+// thread, one wave of resident blocks.
 //
 // Quantisation rules are those of the workload definition (MXFP8: E8M0 scale
 // 2^ceil(log2(amax/448)) per 1x32 block, E4M3 RNE saturating; NVFP4: FP32
 // tensor scale amax/(6*448), E4M3 block scale blockamax/(6*tensor scale) per
 // 1x16 block, E2M1 RNE), for the MXFP8/NVFP4 formats of "ThunderKittens 2.0
 // GPU Kernel优化" (table of updates).  Every FP32 step is one IEEE operation
-// with round-to-nearest (explicit __f*_rn intrinsics, never contracted).
+// with round-to-nearest (explicit __f*_rn intrinsics, never contracted); the
+// NVFP4 element quotients take a shortcut that provably gives the same codes
+// (e2m1_quotients).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -56,35 +58,46 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// Work layout shared by both quantisers: a warp pass covers 512 contiguous
-// bytes of X (lane l loads the float4 at 16*l), i.e. four 32-element MXFP8
-// blocks or eight 16-element NVFP4 blocks.  Each warp takes kUnroll
-// consecutive passes per loop trip and issues all their loads before any
-// arithmetic, so that every SM keeps enough bytes in flight to cover the HBM
-// latency.  When k/bs is a multiple of 4, the four scale bytes of blocks
-// kb..kb+3 (kb % 4 == 0) of a row are adjacent in the tiled layout and go out
-// as one 32-bit store.
-constexpr int kUnroll = 4;
+// Each warp walks its own contiguous range of passes, and every lane keeps the
+// (row, K-block) of the block it works on up to date by addition, so the loop
+// holds no integer division.  When k/bs is a multiple of 4, the four scale
+// bytes of blocks kb..kb+3 (kb % 4 == 0) of a row are adjacent in the tiled
+// layout and go out as one 32-bit store.
+struct WarpRange {
+  long long p0, p1;   // passes [p0, p1) of this warp
+};
+__device__ __forceinline__ WarpRange warp_range(long long passes, int unroll) {
+  const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long per = ((passes + nwarps - 1) / nwarps + unroll - 1) / unroll * unroll;
+  const long long p0 = warp * per;
+  return {p0, p0 + per < passes ? p0 + per : passes};
+}
+
+// MXFP8: a warp pass covers 512 contiguous bytes of X (lane l loads the float4
+// at 16*l), four 32-element blocks; the block amax meets over 8 lanes.  Four
+// passes per loop trip, all loads issued before any arithmetic.
+constexpr int kMxUnroll = 4;
 
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kblk, const float* __restrict__ X,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
                                                           int ka) {
   const int lane = threadIdx.x & 31;
-  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const long long passes = (nblk + 3) / 4;
+  const WarpRange wr = warp_range((nblk + 3) / 4, kMxUnroll);
+  if (wr.p0 >= wr.p1) return;
   const bool packed_sf = (kblk & 3) == 0;
-  for (long long w = warp0 * kUnroll; w < passes; w += nwarps * kUnroll) {
-    float4 x[kUnroll];
+  long long b = wr.p0 * 4 + (lane >> 3);   // this lane's block
+  int r = int(b / kblk), kb = int(b - (long long)r * kblk);
+  for (long long p = wr.p0; p < wr.p1; p += kMxUnroll) {
+    float4 x[kMxUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long b = (w + u) * 4 + (lane >> 3);
-      x[u] = b < nblk ? __ldcs(reinterpret_cast<const float4*>(X + b * 32 + 4 * (lane & 7)))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kMxUnroll; ++u) {
+      const long long bu = b + 4 * u;
+      x[u] = bu < nblk ? __ldcs(reinterpret_cast<const float4*>(X + bu * 32 + 4 * (lane & 7)))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long b = (w + u) * 4 + (lane >> 3);
+    for (int u = 0; u < kMxUnroll; ++u) {
       float a = fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w)));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
@@ -100,7 +113,6 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kb
         const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[u].x, inv), __fmul_rn(x[u].y, inv));
         const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[u].z, inv), __fmul_rn(x[u].w, inv));
         *reinterpret_cast<uint32_t*>(Q + b * 32 + 4 * (lane & 7)) = lo | (hi << 16);
-        const int r = int(b / kblk), kb = int(b % kblk);
         if (packed_sf) {
           if (lane == 0)
             *reinterpret_cast<uint32_t*>(SF + sf_tiled_offset(r, kb, ka)) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
@@ -108,24 +120,31 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kb
           SF[sf_tiled_offset(r, kb, ka)] = uint8_t(code);
         }
       }
+      b += 4;
+      kb += 4;
+      while (kb >= kblk) {
+        kb -= kblk;
+        ++r;
+      }
     }
   }
 }
 
 // amax over the whole tensor, as the bits of a non-negative float (monotone as unsigned).
+constexpr int kAmaxUnroll = 4;
 __global__ void __launch_bounds__(256) amax_kernel(long long n4, const float* __restrict__ X,
                                                    unsigned int* __restrict__ out) {
   float a = 0.f;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i0 < n4; i0 += stride * kUnroll) {
-    float4 x[kUnroll];
+  for (long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i0 < n4; i0 += stride * kAmaxUnroll) {
+    float4 x[kAmaxUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kAmaxUnroll; ++u) {
       const long long i = i0 + u * stride;
       x[u] = i < n4 ? __ldg(reinterpret_cast<const float4*>(X) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
+    for (int u = 0; u < kAmaxUnroll; ++u)
       a = fmaxf(a, fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w))));
   }
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -145,55 +164,98 @@ __global__ void tensor_scale_kernel(unsigned int* __restrict__ word) {
   *reinterpret_cast<float*>(word) = __fdiv_rn(amax, 2688.0f);
 }
 
+// E2M1 codes of x0/den and x1/den (IEEE quotients), `x0` in the low nibble.
+// The quotient is first taken as x * rcp.approx(den): rcp.approx is within 1
+// ulp of 1/den for the normal den given here, so x * r lies within about 2^-22
+// (relative) of the correctly rounded quotient.  Rounding to E2M1 is monotone,
+// so if q * (1 - 2^-18) and q * (1 + 2^-18) round to the same code, so does the
+// IEEE quotient, which lies between them; otherwise (a quotient within 2^-18 of
+// a rounding boundary, where a tie may be at stake) the IEEE division decides.
+__device__ __forceinline__ uint32_t e2m1_quotients(float x0, float x1, float den, float r) {
+  const float q0 = x0 * r, q1 = x1 * r;
+  constexpr float kLo = 1.0f - 1.0f / 262144.0f, kHi = 1.0f + 1.0f / 262144.0f;
+  const uint32_t c_lo = cvt_e2m1x2(q0 * kLo, q1 * kLo);
+  const uint32_t c_hi = cvt_e2m1x2(q0 * kHi, q1 * kHi);
+  if (c_lo == c_hi) return c_lo;
+  return cvt_e2m1x2(__fdiv_rn(x0, den), __fdiv_rn(x1, den));
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// NVFP4: one lane per 16-element block (its 64 bytes in four float4 loads), so
+// the block amax, the block scale and the reciprocal are computed once per
+// block; a warp pass covers 32 consecutive blocks (2 KB of X), two passes per
+// loop trip.
+constexpr int kNvUnroll = 2;
+
 __global__ void __launch_bounds__(256) quant_nvfp4_kernel(long long nblk, int kblk, const float* __restrict__ X,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF, int ka,
                                                           const float* __restrict__ tptr) {
   const int lane = threadIdx.x & 31;
-  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const long long passes = (nblk + 7) / 8;
+  const WarpRange wr = warp_range((nblk + 31) / 32, kNvUnroll);
+  if (wr.p0 >= wr.p1) return;
   const bool packed_sf = (kblk & 3) == 0;
   const float t = __ldg(tptr);
   const float d = __fmul_rn(6.0f, t);
-  for (long long w = warp0 * kUnroll; w < passes; w += nwarps * kUnroll) {
-    float4 x[kUnroll];
+  long long b = wr.p0 * 32 + lane;   // this lane's block
+  int r = int(b / kblk), kb = int(b - (long long)r * kblk);
+  for (long long p = wr.p0; p < wr.p1; p += kNvUnroll) {
+    float4 x[kNvUnroll][4];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long b = (w + u) * 8 + (lane >> 2);
-      x[u] = b < nblk ? __ldcs(reinterpret_cast<const float4*>(X + b * 16 + 4 * (lane & 3)))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kNvUnroll; ++u) {
+      const long long bu = b + 32 * u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        x[u][j] = bu < nblk ? __ldcs(reinterpret_cast<const float4*>(X + bu * 16) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long b = (w + u) * 8 + (lane >> 2);
-      float a = fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w)));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    for (int u = 0; u < kNvUnroll; ++u) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(x[u][j].x), fabsf(x[u][j].y)), fmaxf(fabsf(x[u][j].z), fabsf(x[u][j].w))));
       uint32_t s = 0;
       float den = 0.f;
       if (t > 0.f) {
         s = cvt_e4m3x2(__fdiv_rn(a, d), 0.f) & 0xFFu;
         den = __fmul_rn(e4m3_value(s), t);
       }
-      // scale bytes of blocks j..j+3 gathered in lanes 0 and 16
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 4);
-      const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 8);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 12);
+      // scale bytes of blocks kb..kb+3, gathered in lanes 0, 4, ...
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, s, 1);
+      const uint32_t s2 = __shfl_down_sync(0xffffffffu, s, 2);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, s, 3);
       if (b < nblk) {
-        uint32_t packed = 0;
+        uint32_t w[2] = {0u, 0u};
         if (den > 0.f) {
-          const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x[u].x, den), __fdiv_rn(x[u].y, den));
-          const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x[u].z, den), __fdiv_rn(x[u].w, den));
-          packed = lo | (hi << 8);
+          // 2^-124 <= den keeps 1/den a finite normal float
+          const bool fast = den >= 4.7019774e-38f;
+          const float rr = rcp_approx(den);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = fast ? e2m1_quotients(x[u][j].x, x[u][j].y, den, rr)
+                                     : cvt_e2m1x2(__fdiv_rn(x[u][j].x, den), __fdiv_rn(x[u][j].y, den));
+            const uint32_t hi = fast ? e2m1_quotients(x[u][j].z, x[u][j].w, den, rr)
+                                     : cvt_e2m1x2(__fdiv_rn(x[u][j].z, den), __fdiv_rn(x[u][j].w, den));
+            w[j >> 1] |= (lo | (hi << 8)) << (16 * (j & 1));
+          }
         }
-        *reinterpret_cast<uint16_t*>(Q + b * 8 + 2 * (lane & 3)) = uint16_t(packed);
-        const int r = int(b / kblk), kb = int(b % kblk);
+        *reinterpret_cast<uint2*>(Q + b * 8) = make_uint2(w[0], w[1]);
         if (packed_sf) {
-          if ((lane & 15) == 0)
+          if ((lane & 3) == 0)
             *reinterpret_cast<uint32_t*>(SF + sf_tiled_offset(r, kb, ka)) = s | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        } else if ((lane & 3) == 0) {
+        } else {
           SF[sf_tiled_offset(r, kb, ka)] = uint8_t(s);
         }
+      }
+      b += 32;
+      kb += 32;
+      while (kb >= kblk) {
+        kb -= kblk;
+        ++r;
       }
     }
   }
@@ -243,7 +305,7 @@ tkg_status tkg_quantize_mxfp8(int rows, int k, const float* X, void* Q, void* sf
   const int kblk = k / 32, ka = (kblk + 3) / 4;
   if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 32), stream) != cudaSuccess) return TKG_ERR_CUDA;
   const long long nblk = (long long)rows * kblk;
-  const int grid = grid_for(quant_mxfp8_kernel, ((nblk + 3) / 4 + kUnroll - 1) / kUnroll * 32, 256);
+  const int grid = grid_for(quant_mxfp8_kernel, ((nblk + 3) / 4 + kMxUnroll - 1) / kMxUnroll * 32, 256);
   quant_mxfp8_kernel<<<grid, 256, 0, stream>>>(
       nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
@@ -262,10 +324,10 @@ tkg_status tkg_quantize_nvfp4(int rows, int k, const float* X, void* Q, void* sf
   if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 16), stream) != cudaSuccess) return TKG_ERR_CUDA;
   unsigned int* word = reinterpret_cast<unsigned int*>(tensor_scale);
   const long long n4 = (long long)rows * k / 4;
-  amax_kernel<<<grid_for(amax_kernel, (n4 + kUnroll - 1) / kUnroll, 256), 256, 0, stream>>>(n4, X, word);
+  amax_kernel<<<grid_for(amax_kernel, (n4 + kAmaxUnroll - 1) / kAmaxUnroll, 256), 256, 0, stream>>>(n4, X, word);
   tensor_scale_kernel<<<1, 1, 0, stream>>>(word);
   const long long nblk = (long long)rows * kblk;
-  const int grid = grid_for(quant_nvfp4_kernel, ((nblk + 7) / 8 + kUnroll - 1) / kUnroll * 32, 256);
+  const int grid = grid_for(quant_nvfp4_kernel, ((nblk + 31) / 32 + kNvUnroll - 1) / kNvUnroll * 32, 256);
   quant_nvfp4_kernel<<<grid, 256, 0, stream>>>(
       nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka, tensor_scale);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;

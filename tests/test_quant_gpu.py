@@ -62,3 +62,44 @@ def test_scales_to_tiled_bit_exact(rows, kb):
     dst = torch.full((-(-rows // 128) * 128 * (-(-kb // 4)) * 4,), 0x33, dtype=torch.uint8, device="cuda")
     tkg.scales_to_tiled(to_dev(src), dst, kblocks=kb)
     assert np.array_equal(dst.cpu().numpy(), tiled_scales(src, kb))
+
+
+def _boundary_blocks(rows, k, seed):
+    """FP32 input whose element quotients x / den fall exactly on, and a few ulps
+    either side of, every E2M1 rounding boundary (0.25, 0.75, ..., 5).
+
+    t = 2^-10 and block 0 holds 6 * 448 * t, so the tensor scale is exactly t;
+    each block's maximum is 6 * dec(s) * t for a chosen E4M3 code s, so the block
+    scale decodes to dec(s) and den = dec(s) * t, all exact in FP32."""
+    rng = np.random.default_rng(seed)
+    e4m3 = oracle.decode_table("e4m3")
+    t = np.float32(2.0 ** -10)
+    bounds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+    nb = rows * k // 16
+    codes = rng.integers(8, 108, size=nb)
+    codes[0] = 0x7E                                          # 448: the tensor maximum
+    den = (e4m3[codes] * float(t)).astype(np.float32)
+    x = np.empty((nb, 16), dtype=np.float32)
+    x[:, 0] = np.float32(6.0) * den
+    base = bounds[rng.integers(0, 7, size=(nb, 15))] * den[:, None]
+    ulps = rng.integers(-4, 5, size=(nb, 15)).astype(np.int32)
+    x[:, 1:] = (base.view(np.int32) + ulps).view(np.float32)
+    x[:, 1:] *= np.where(rng.integers(0, 2, size=(nb, 15)) == 1, np.float32(-1), np.float32(1))
+    return x.reshape(rows, k)
+
+
+@pytest.mark.parametrize("rows,k", [(64, 1024), (40, 96)])
+def test_quantize_nvfp4_rounding_boundaries(rows, k):
+    # quotients on and next to every E2M1 tie, each side of zero: the kernel's
+    # fast quotient must fall back to the IEEE division exactly where needed
+    x = _boundary_blocks(rows, k, seed=rows * k)
+    Q_ref, SF_ref, t_ref = oracle.quant_nvfp4(x)
+    assert float(t_ref) == 2.0 ** -10
+    X = to_dev(x)
+    Q = torch.empty((rows, k // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.full((tkg.scale_bytes(rows, k, 16),), 0xEE, dtype=torch.uint8, device="cuda")
+    t = torch.empty(1, dtype=torch.float32, device="cuda")
+    tkg.quantize_nvfp4(X, Q, SF, t)
+    assert t.item() == float(t_ref)
+    assert np.array_equal(Q.cpu().numpy(), Q_ref)
+    assert np.array_equal(SF.cpu().numpy(), tiled_scales(SF_ref, k // 16))
