@@ -280,8 +280,27 @@ __global__ void __launch_bounds__(384, 1)
   if (CG == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+  // Warm L2 with the first stages of this cluster's first tile while the
+  // previous kernel may still be running (prefetches read nothing back; see
+  // ptx::tma_prefetch_2d).
+  if (warp == 0) {
+    if (ptx::elect_one() && int(blockIdx.x) / CG < p.num_tiles) {
+      int mb, nb;
+      tile_coords(int(blockIdx.x) / CG, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+      const int a_row = mb * C::kMmaM + int(rank) * C::kCtaM;
+      const int b_row = nb * BN + int(rank) * C::kBRows;
+      const int npf = min(p.num_kstages, STAGES);
+#pragma unroll 1
+      for (int ks = 0; ks < npf; ++ks) {
+        const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
+        ptx::tma_prefetch_2d(&tmA, kx, a_row);
+        ptx::tma_prefetch_2d(&tmB, kx, b_row);
+      }
+    }
+    __syncwarp();
+  }
   // Programmatic dependent launch: the set-up above overlapped the previous
-  // kernel's tail; global memory is touched only after it has completed.  The
+  // kernel's tail; global memory is read only after it has completed.  The
   // next kernel may start its own set-up as soon as SMs free up.
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();

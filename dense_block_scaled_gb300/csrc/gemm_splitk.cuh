@@ -4,10 +4,11 @@
 // 128 x 128, fewer than half the SMs, and is bound by HBM reads of B.  Here a
 // cluster of SPLIT CTAs works on one 128 x 128 tile, each CTA on its own
 // stretch of K, so SPLIT times as many SMs stream B.  The partial
-// accumulators meet in the cluster leader's shared memory (distributed shared
-// memory, no global scratch): once every CTA's MMAs are done, the others write
-// their FP32 partials into the leader's now idle stage buffers, and the leader
-// adds them, scales by alpha, rounds to BF16 and stores D.
+// accumulators meet in shared memory (distributed shared memory, no global
+// scratch): each 32-row quadrant of the tile belongs to one CTA of the
+// cluster; once a CTA's MMAs are done, the others write their FP32 partials of
+// its quadrants into its now idle stage buffers, and it adds them, scales by
+// alpha, rounds to BF16 and stores those rows of D.
 //
 // Same operand formats, layouts, roles and bounded waits as gemm_kernel.cuh;
 // single-CTA MMAs (M = 128, N = 128) and one tile per cluster.
@@ -18,8 +19,8 @@
 // buys a deeper pipeline for the B stream.
 //
 // The partials move with st.async, which counts its bytes on an mbarrier in
-// the leader; the leader tells the others that its stage buffers are free by a
-// relaxed remote arrive.  No cluster-wide barrier sits on the path.
+// the receiving CTA; each CTA tells the others that its stage buffers are free
+// by a relaxed remote arrive.  No cluster-wide barrier sits on the path.
 #pragma once
 #include "gemm_kernel.cuh"
 
@@ -61,6 +62,7 @@ struct SplitKConfig {
   static constexpr int kRegionCols = 8;                  // 4 columns of A scales, 4 of B scales
   static constexpr int kRegions = (512 - BN) / kRegionCols;
   static constexpr int kTmemCols = 512;
+  static constexpr int kPrefetchStages = 4;   // L2 prefetch ahead of the dependency wait (deeper delays the real loads)
   static_assert(SPLIT >= 1 && SPLIT <= 4, "split factor");
   static_assert(AROWS == 128 || AROWS == 32, "A tile height");
   // the MMA's 128-row read of a short A tile stays inside its stage
@@ -86,7 +88,6 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = (SPLIT > 1) ? ptx::cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
 
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -103,8 +104,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t accf_bar = bars + uint32_t(8 * (2 * STAGES));
   const uint32_t drain_bar = accf_bar + 8;
   const uint32_t never_bar = drain_bar + 8;
-  const uint32_t go_bar = never_bar + 8;     // others: the leader's stage buffers are free
-  const uint32_t part_bar = go_bar + 8;      // leader: all partial bytes have landed
+  const uint32_t go_bar = never_bar + 8;     // every other CTA's stage buffers are free
+  const uint32_t part_bar = go_bar + 8;      // all partial bytes for this CTA's quadrants have landed
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(384, 1)
     ptx::mbar_init(accf_bar, 1);
     ptx::mbar_init(drain_bar, 1);
     ptx::mbar_init(never_bar, 1);
-    ptx::mbar_init(go_bar, 1);
+    ptx::mbar_init(go_bar, SPLIT > 1 ? SPLIT - 1 : 1);
     ptx::mbar_init(part_bar, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
@@ -135,8 +136,35 @@ __global__ void __launch_bounds__(384, 1)
   if (SPLIT > 1) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = s_tmem_base;
+
+  int mb, nb;
+  tile_coords(int(blockIdx.x) / SPLIT, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
+  // this CTA's stretch of K (in stages); the host keeps every stretch non-empty
+  const int per = (p.num_kstages + SPLIT - 1) / SPLIT;
+  const int ks0 = int(rank) * per;
+  const int ks1 = min(ks0 + per, p.num_kstages);
+
+  // Warm L2 with the first stages of this CTA's stretch while the previous
+  // kernel may still be running (prefetches read nothing back; see
+  // ptx::tma_prefetch_2d).
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      const int npf = min(ks1 - ks0, C::kPrefetchStages);
+#pragma unroll 1
+      for (int ks = ks0; ks < ks0 + npf; ++ks) {
+        const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
+        ptx::tma_prefetch_2d(&tmB, kx, nb * C::BN);
+        ptx::tma_prefetch_2d(&tmA, kx, mb * C::BM);
+        if constexpr (C::kScaled) {
+          ptx::tma_prefetch_3d(&tmSFB, 0, ks * T::kSfAtoms, nb);
+          ptx::tma_prefetch_3d(&tmSFA, 0, ks * T::kSfAtoms, mb);
+        }
+      }
+    }
+    __syncwarp();
+  }
   // Programmatic dependent launch: the set-up above overlapped the previous
-  // kernel's tail; global memory is touched only after it has completed.  The
+  // kernel's tail; global memory is read only after it has completed.  The
   // next kernel may start its own set-up as soon as SMs free up.
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
@@ -148,13 +176,6 @@ __global__ void __launch_bounds__(384, 1)
   ctl.ncta = SPLIT;
   ctl.status = p.status;
   ctl.timeout_ns = p.timeout_ns;
-
-  int mb, nb;
-  tile_coords(int(blockIdx.x) / SPLIT, p.tiles_m, p.tiles_n, p.raster_group, mb, nb);
-  // this CTA's stretch of K (in stages); the host keeps every stretch non-empty
-  const int per = (p.num_kstages + SPLIT - 1) / SPLIT;
-  const int ks0 = int(rank) * per;
-  const int ks1 = min(ks0 + per, p.num_kstages);
 
   // ------------------------------------------------------------------ producer
   if (warp == 0) {
@@ -279,27 +300,49 @@ __global__ void __launch_bounds__(384, 1)
   };
 
   // ------------------------------------------------------------------ split-K reduction
+  // Quadrant q of the tile is summed and stored by CTA q * SPLIT / 4 (with two
+  // CTAs: rows 0-63 by the first, 64-127 by the second), so the partial traffic
+  // and the final epilogue are spread over the cluster.
+  const int owner = (q * SPLIT) / 4;
+  const bool mine = owner == int(rank);
   if constexpr (SPLIT > 1) {
-    // quadrants with rows below M; each of their warps moves 32 rows x 64 columns
     const int rows_left = p.m - mb * C::BM;
     const int live_q = rows_left >= C::BM ? 4 : (rows_left + 31) / 32;
-    const uint32_t part_bytes = uint32_t((SPLIT - 1) * live_q * 2) * uint32_t(32 * 64 * 4);
-    if (leader) {
-      if (warp == 4 && lane == 0 && have) {
-        // every MMA of this CTA has completed, so its stage buffers are free
-        ptx::mbar_arrive_expect_tx(part_bar, part_bytes);
+    int my_live = 0;   // quadrants with rows below M that this CTA owns
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) my_live += (qq < live_q && (qq * SPLIT) / 4 == int(rank)) ? 1 : 0;
+    const uint32_t part_bytes = uint32_t((SPLIT - 1) * my_live * 2) * uint32_t(32 * 64 * 4);
+    if (warp == 4 && lane == 0 && have) {
+      // every MMA of this CTA has completed, so its stage buffers may take partials
+      ptx::mbar_arrive_expect_tx(part_bar, part_bytes);
 #pragma unroll 1
-        for (uint32_t r = 1; r < uint32_t(SPLIT); ++r) ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(go_bar, r));
+      for (uint32_t r = 0; r < uint32_t(SPLIT); ++r)
+        if (r != rank) ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(go_bar, r));
+    }
+    if (epi && have && !mine) {
+      uint32_t ok = 0;
+      if (lane == 0) ok = wait_bar<false>(go_bar, 0u, ctl) ? 1u : 0u;
+      if (__shfl_sync(0xffffffffu, ok, 0)) {
+        const int slot = int(rank) < owner ? int(rank) : int(rank) - 1;   // this CTA's place among the senders
+        const uint32_t dst = ptx::map_to_rank(base + uint32_t(slot * C::kPartialBytes), uint32_t(owner));
+        const uint32_t rbar = ptx::map_to_rank(part_bar, uint32_t(owner));
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t a = dst + uint32_t(row * 512) + uint32_t((((h * 16 + c * 8 + j) ^ row) & 31) * 16);
+            st_async_v4(a, v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3], rbar);
+          }
       }
-      if (epi && have) {
-        uint32_t ok = 0;
-        if (lane == 0) ok = wait_bar<false>(part_bar, 0u, ctl) ? 1u : 0u;
-        have = __shfl_sync(0xffffffffu, ok, 0);
-      }
-      if (epi && have) {
+    }
+    if (epi && have && mine) {
+      uint32_t ok = 0;
+      if (lane == 0) ok = wait_bar<false>(part_bar, 0u, ctl) ? 1u : 0u;
+      have = __shfl_sync(0xffffffffu, ok, 0);
+      if (have) {
 #pragma unroll 1
-        for (int r = 1; r < SPLIT; ++r) {
-          const uint32_t src = base + uint32_t((r - 1) * C::kPartialBytes);
+        for (int r = 0; r < SPLIT - 1; ++r) {
+          const uint32_t src = base + uint32_t(r * C::kPartialBytes);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -315,25 +358,11 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
       }
-    } else if (epi && have) {
-      uint32_t ok = 0;
-      if (lane == 0) ok = wait_bar<false>(go_bar, 0u, ctl) ? 1u : 0u;
-      if (__shfl_sync(0xffffffffu, ok, 0)) {
-        const uint32_t dst = ptx::map_to_rank(base + uint32_t((rank - 1) * C::kPartialBytes), 0);
-        const uint32_t rbar = ptx::map_to_rank(part_bar, 0);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t a = dst + uint32_t(row * 512) + uint32_t((((h * 16 + c * 8 + j) ^ row) & 31) * 16);
-            st_async_v4(a, v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2], v[c][4 * j + 3], rbar);
-          }
-      }
     }
   }
 
-  // ------------------------------------------------------------------ epilogue: leader stores D
-  if (epi && leader && have && !s_abort) {
+  // ------------------------------------------------------------------ epilogue: the owner stores D
+  if (epi && mine && have && !s_abort) {
     float alpha = p.alpha;
     if (p.ta) alpha = alpha * __ldg(p.ta);
     if (p.tb) alpha = alpha * __ldg(p.tb);
