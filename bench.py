@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantiser timings")
+    ap.add_argument("--grouped", default="8,16384,4096,7168",
+                    help="grouped GEMM reported beside the headline: groups,total rows,N,K ('' to skip)")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
     return ap.parse_args()
 
@@ -271,6 +273,80 @@ def quant_timings(X, steps, warmup, torch, tkg, hbm_gbs):
     return out
 
 
+GROUPED_SEED = 1006
+
+
+def grouped_sizes(groups, total, seed=GROUPED_SEED):
+    """Group row counts of the mixture-of-experts workload: `total` rows dealt
+    to `groups` experts by a seeded multinomial draw, in whole 128-row blocks
+    (the padded layout in which each group starts on a scale block)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return [int(x) * 128 for x in rng.multinomial(total // 128, [1.0 / groups] * groups)]
+
+
+def grouped_timings(formats, groups, total, n, k, steps, warmup, torch, tkg, synth):
+    """TFLOP/s of the grouped GEMM over `groups` experts of n x k weights.
+    Inputs are seeded N(0,1); MXFP8 / NVFP4 operands come from the library's
+    quantisers (A as one tensor: with 128-row groups its tiled scales are the
+    per-group layout; each expert's B as its own tensor)."""
+    sizes = grouped_sizes(groups, total)
+    a, b = synth.gemm_inputs_f32(total, groups * n, k, GROUPED_SEED)
+    dev = torch.device("cuda")
+    out = {"sizes": sizes, "n": n, "k": k}
+    flop = 2.0 * total * n * k
+    for fmt in formats:
+        D = torch.empty((total, n), dtype=torch.bfloat16, device=dev)
+        if fmt == "bf16":
+            A = torch.from_numpy(synth.bf16_codes(a).view("int16")).view(torch.bfloat16).to(dev)
+            B = torch.from_numpy(synth.bf16_codes(b).view("int16")).view(torch.bfloat16).to(dev).view(groups, n, k)
+            run = lambda: tkg.gemm_grouped_bf16(sizes, A, B, D)
+        else:
+            bs = 32 if fmt == "mxfp8" else 16
+            cols = k if fmt == "mxfp8" else k // 2
+            X = torch.from_numpy(a).to(dev)
+            A = torch.empty((total, cols), dtype=torch.uint8, device=dev)
+            SA = torch.empty((tkg.scale_bytes(total, k, bs),), dtype=torch.uint8, device=dev)
+            B = torch.empty((groups, n, cols), dtype=torch.uint8, device=dev)
+            sfb_g = tkg.scale_bytes(n, k, bs)
+            SB = torch.empty((groups * sfb_g,), dtype=torch.uint8, device=dev)
+            TA = torch.empty(1, dtype=torch.float32, device=dev)
+            TB = torch.empty(groups, dtype=torch.float32, device=dev)
+            if fmt == "mxfp8":
+                tkg.quantize_mxfp8(X, A, SA)
+            else:
+                tkg.quantize_nvfp4(X, A, SA, TA)
+            del X
+            for g in range(groups):
+                Y = torch.from_numpy(b[g * n:(g + 1) * n]).to(dev)
+                if fmt == "mxfp8":
+                    tkg.quantize_mxfp8(Y, B[g], SB[g * sfb_g:(g + 1) * sfb_g])
+                else:
+                    tkg.quantize_nvfp4(Y, B[g], SB[g * sfb_g:(g + 1) * sfb_g], TB[g:g + 1])
+            if fmt == "mxfp8":
+                run = lambda: tkg.gemm_grouped_mxfp8(sizes, A, B, SA, SB, D)
+            else:
+                run = lambda: tkg.gemm_grouped_nvfp4(sizes, A, B, SA, SB, D, ta=TA, tb=TB)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        if tkg.device_status() != tkg.OK:
+            raise RuntimeError("device status after grouped timing")
+        out[fmt] = {"us": t * 1e6, "tflops": flop / t / 1e12,
+                    "frac_of_pages_peak": flop / t / 1e12 / PAGES_PEAK_TFLOPS[fmt]}
+        del A, B, D
+        torch.cuda.empty_cache()
+    return out
+
+
 def graph_seconds(w, steps, torch, tkg):
     """Seconds per launch when the K launches are replayed from one captured CUDA
     graph: the same kernels without the per-call host work."""
@@ -438,7 +514,7 @@ def run_ours(args):
                 "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
                 "measured_peak_tflops": peak_meas, "input_groups": w.groups}
 
-    by_format, sweep, skinny, quant = {}, {}, {}, {}
+    by_format, sweep, skinny, quant, grouped = {}, {}, {}, {}, {}
     e2e = None
     if rank == 0:
         by_format[hf] = fmt_entry(head, t_head)
@@ -476,6 +552,10 @@ def run_ours(args):
                     "us_graph": tg * 1e6, "frac_of_roofline_graph": w.flop / tg / 1e12 / roof}
                 del w
                 torch.cuda.empty_cache()
+        if args.grouped:
+            gg, gt, gn, gk = [int(x) for x in args.grouped.split(",")]
+            grouped = grouped_timings([f for f in ("bf16", "mxfp8", "nvfp4")], gg, gt, gn, gk,
+                                      min(args.steps, 50), min(args.warmup, 20), torch, tkg, synth)
         if not args.no_e2e:
             te, h2d, d2h = e2e_seconds(head, args.e2e_steps, torch, tkg)
             e2e = {"value": world * head.flop / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -511,6 +591,7 @@ def run_ours(args):
             "sweep_bf16": sweep,
             "skinny": skinny,
             "quantize": quant,
+            "grouped": grouped,
             "kernel_hash": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

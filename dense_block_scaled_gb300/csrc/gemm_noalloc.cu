@@ -140,7 +140,7 @@ extern "C" tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void* A, 
 
   // The array keeps the previous call's contents: the status word must start at zero.
   if (cudaMemsetAsync(p.status, 0, kScratchNeeded, stream) != cudaSuccess) return TKG_ERR_CUDA;
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, tmD, tmD, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, tmD, tmD, p, NoGroups{0}) != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;
   }

@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(384, 1)
   // ------------------------------------------------------------------ producer
   if (warp == 0) {
     if (ptx::elect_one()) {
-      const uint64_t pol_a = ptx::policy_evict_last();
-      const uint64_t pol_b = ptx::policy_evict_normal();
+      const uint64_t pol_a = ptx::policy_evict_last();    // A is read by every N tile
+      const uint64_t pol_b = ptx::policy_evict_first();   // B is read once
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
 #pragma unroll 1

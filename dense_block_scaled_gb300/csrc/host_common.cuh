@@ -15,15 +15,17 @@
 namespace tkg {
 
 struct Problem {
-  int m, n, k;
+  int m, n, k;               // grouped: m = rows of A and D (at least the sum of the group sizes)
   const void* A;
   const void* B;
   const void* sfa;
   const void* sfb;
   const float* ta;
-  const float* tb;
+  const float* tb;           // grouped NVFP4: one per group
   void* D;
   float alpha;
+  int groups = 0;            // grouped GEMM: number of groups, and their sizes (host)
+  const int* m_sizes = nullptr;
 };
 
 // ---- options and per-device state (tkg_api.cu)
@@ -59,12 +61,13 @@ tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Launch one instantiation of the persistent GEMM.
-template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED>
+// Launch one instantiation of the persistent GEMM (or, with GROUPED, of the
+// grouped GEMM over pr.groups groups of rows).
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED, bool GROUPED = false>
 tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
-  auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC, SCHED>;
+  auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC, SCHED, GROUPED>;
   // Request at least just over half an SM's shared memory so that no two CTAs
   // ever share an SM: each allocates all 512 tensor-memory columns.
   constexpr int kLaunchSmem = C::kSmemBytes > 118784 ? C::kSmemBytes : 118784;
@@ -81,6 +84,41 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
     attr_set[dev] = true;
   }
 
+  // group table: tiles, rows and scale blocks of each group
+  std::conditional_t<GROUPED, GroupTable, NoGroups> gt{};
+  int b_rows = pr.n, sfa_blocks = ceil_div(pr.m, 128), sfb_blocks = ceil_div(pr.n, 128);
+  int total_tiles = ceil_div(pr.m, C::kMmaM) * ceil_div(pr.n, BN), max_tiles_m = ceil_div(pr.m, C::kMmaM);
+  if constexpr (GROUPED) {
+    if (pr.groups < 1 || pr.groups > kMaxGroups || !pr.m_sizes) return TKG_ERR_INVALID_ARG;
+    const int tiles_n = ceil_div(pr.n, BN);
+    gt.count = pr.groups;
+    gt.n_blocks = ceil_div(pr.n, 128);
+    gt.ldd = pr.n;
+    gt.d = pr.D;
+    gt.tb = pr.tb;
+    long long row = 0, blk = 0, tiles = 0;
+    max_tiles_m = 1;
+    for (int g = 0; g < pr.groups; ++g) {
+      const int mg = pr.m_sizes[g];
+      gt.tile_start[g] = int(tiles);
+      gt.row0[g] = int(row);
+      gt.rows[g] = mg;
+      gt.sfa_block0[g] = int(blk);
+      const int tm = ceil_div(mg, C::kMmaM);
+      if (tm > max_tiles_m) max_tiles_m = tm;
+      tiles += (long long)tm * tiles_n;
+      row += mg;
+      blk += ceil_div(mg, 128);
+    }
+    gt.tile_start[pr.groups] = int(tiles);
+    if (row > pr.m || tiles > 0x7fffffff) return TKG_ERR_INVALID_ARG;
+    b_rows = pr.groups * pr.n;
+    sfa_blocks = int(blk) > 0 ? int(blk) : 1;
+    sfb_blocks = pr.groups * gt.n_blocks;
+    total_tiles = int(tiles);
+    if (total_tiles == 0) return TKG_OK;
+  }
+
   // operand tensor maps: 128-byte K rows per stage, 128-byte swizzle
   CUtensorMap tmA, tmB, tmSFA, tmSFB, tmD;
   const bool bf16 = FMT == FMT_BF16;
@@ -91,7 +129,8 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   tkg_status st;
   if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
@@ -99,10 +138,10 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if constexpr (C::kScaled) {
     const int bs = FMT == FMT_MXFP8 ? 32 : 16;
     const int ka = ceil_div(ceil_div(pr.k, bs), 4);   // 512-byte atoms per 128-row block
-    if ((st = encode_3d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfa, 128, ka, ceil_div(pr.m, 128), 512,
+    if ((st = encode_3d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfa, 128, ka, sfa_blocks, 512,
                         uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
       return st;
-    if ((st = encode_3d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfb, 128, ka, ceil_div(pr.n, 128), 512,
+    if ((st = encode_3d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, pr.sfb, 128, ka, sfb_blocks, 512,
                         uint64_t(ka) * 512, 128, T::kSfAtoms, 1)) != TKG_OK)
       return st;
   } else {
@@ -117,15 +156,15 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   p.num_kstages = ceil_div(pr.k, T::kStageK);
   p.tiles_m = ceil_div(pr.m, C::kMmaM);
   p.tiles_n = ceil_div(pr.n, BN);
-  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_tiles = total_tiles;
   p.alpha = pr.alpha;
   p.ta = pr.ta;
-  p.tb = pr.tb;
+  p.tb = GROUPED ? nullptr : pr.tb;
   if ((st = device_status_word(&p.status)) != TKG_OK) return st;
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
-  p.raster_group = raster_group(C::kMmaM, pr.k, FMT, p.tiles_m);
+  p.raster_group = raster_group(C::kMmaM, pr.k, FMT, max_tiles_m);
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;
@@ -173,7 +212,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if (SCHED == SCHED_CLC) clusters = p.num_tiles;
   cfg.gridDim = dim3(clusters * CG, 1, 1);
 
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p, gt);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;
@@ -281,14 +320,17 @@ inline int choose_split(const Problem& pr, int stage_k) {
 }
 
 // Cluster launch control unless TKG_OPT_SCHEDULER asks for the static schedule.
-template <int FMT, int CG, int BN, int STAGES, int ACC>
+template <int FMT, int CG, int BN, int STAGES, int ACC, bool GROUPED = false>
 tkg_status launch_sched(const Problem& pr, cudaStream_t s) {
-  if (option(TKG_OPT_SCHEDULER) == 1) return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC>(pr, s);
-  return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_CLC>(pr, s);
+  if (option(TKG_OPT_SCHEDULER) == 1) return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC, GROUPED>(pr, s);
+  return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_CLC, GROUPED>(pr, s);
 }
 
 tkg_status launch_bf16(const Problem& pr, cudaStream_t s);
 tkg_status launch_mxfp8(const Problem& pr, cudaStream_t s);
 tkg_status launch_nvfp4(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_bf16(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_mxfp8(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_nvfp4(const Problem& pr, cudaStream_t s);
 
 }  // namespace tkg

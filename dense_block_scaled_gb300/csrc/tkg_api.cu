@@ -178,6 +178,28 @@ static tkg_status check_common(int m, int n, int k, const void* A, const void* B
   return TKG_OK;
 }
 
+// Grouped GEMM: checks shared by the three formats.  Sets *rows to the sum of
+// the group sizes and *empty when there is nothing to launch.
+static tkg_status check_grouped(int groups, const int* m_sizes, int n, int k, const void* A, const void* B, void* D,
+                                int k_multiple, int* rows, bool* empty, cudaStream_t stream) {
+  *empty = false;
+  *rows = 0;
+  if (groups < 1 || !m_sizes || n < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (groups > kMaxGroups) return TKG_ERR_UNSUPPORTED;
+  long long total = 0;
+  for (int g = 0; g < groups; ++g) {
+    if (m_sizes[g] < 0) return TKG_ERR_INVALID_ARG;
+    total += m_sizes[g];
+  }
+  if (total > 0x7fffffffLL) return TKG_ERR_UNSUPPORTED;
+  *rows = int(total);
+  if (total == 0 || n == 0) {
+    *empty = true;
+    return TKG_OK;
+  }
+  return check_common(int(total), n, k, A, B, D, k_multiple, empty, stream);
+}
+
 }  // namespace tkg
 
 using namespace tkg;
@@ -217,6 +239,54 @@ tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void* A, const void* B, con
     return TKG_ERR_ALIGNMENT;
   Problem pr{m, n, k, A, B, sfa, sfb, tensor_scale_a, tensor_scale_b, D, alpha};
   return launch_nvfp4(pr, stream);
+}
+
+tkg_status tkg_gemm_grouped_bf16(int groups, const int* m_sizes, int n, int k, const void* A, const void* B, void* D,
+                                 float alpha, cudaStream_t stream) {
+  bool empty;
+  int rows;
+  tkg_status st = check_grouped(groups, m_sizes, n, k, A, B, D, 8, &rows, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  Problem pr{rows, n, k, A, B, nullptr, nullptr, nullptr, nullptr, D, alpha, groups, m_sizes};
+  return launch_grouped_bf16(pr, stream);
+}
+
+tkg_status tkg_gemm_grouped_mxfp8(int groups, const int* m_sizes, int n, int k, const void* A, const void* B,
+                                  const void* sfa, const void* sfb, void* D, float alpha, cudaStream_t stream) {
+  bool empty;
+  int rows;
+  tkg_status st = check_grouped(groups, m_sizes, n, k, A, B, D, 32, &rows, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  Problem pr{rows, n, k, A, B, sfa, sfb, nullptr, nullptr, D, alpha, groups, m_sizes};
+  return launch_grouped_mxfp8(pr, stream);
+}
+
+tkg_status tkg_gemm_grouped_nvfp4(int groups, const int* m_sizes, int n, int k, const void* A, const void* B,
+                                  const void* sfa, const void* sfb, const float* tensor_scale_a,
+                                  const float* tensor_scales_b, void* D, float alpha, cudaStream_t stream) {
+  bool empty;
+  int rows;
+  tkg_status st = check_grouped(groups, m_sizes, n, k, A, B, D, 32, &rows, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  if ((tensor_scale_a && (reinterpret_cast<uintptr_t>(tensor_scale_a) & 3u)) ||
+      (tensor_scales_b && (reinterpret_cast<uintptr_t>(tensor_scales_b) & 3u)))
+    return TKG_ERR_ALIGNMENT;
+  Problem pr{rows, n, k, A, B, sfa, sfb, tensor_scale_a, tensor_scales_b, D, alpha, groups, m_sizes};
+  return launch_grouped_nvfp4(pr, stream);
+}
+
+size_t tkg_grouped_scale_bytes(int groups, const int* m_sizes, int k, int block) {
+  if (groups < 1 || !m_sizes) return 0;
+  size_t total = 0;
+  for (int g = 0; g < groups; ++g) {
+    if (m_sizes[g] < 0) return 0;
+    total += tkg_scale_bytes(m_sizes[g], k, block);
+  }
+  return total;
 }
 
 tkg_status tkg_get_device_status(cudaStream_t stream) {

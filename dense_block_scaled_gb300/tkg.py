@@ -27,6 +27,7 @@ EXPORTS = [
     "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",
     "tkg_scale_bytes", "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
     "tkg_set_option", "tkg_get_option", "tkg_gemm_bf16_noalloc",
+    "tkg_gemm_grouped_bf16", "tkg_gemm_grouped_mxfp8", "tkg_gemm_grouped_nvfp4", "tkg_grouped_scale_bytes",
 ]
 
 _lock = threading.Lock()
@@ -52,6 +53,11 @@ def load() -> ctypes.CDLL:
             lib.tkg_gemm_bf16_noalloc.argtypes = [i, i, i, vp, vp, vp, f, vp]
             lib.tkg_gemm_mxfp8.argtypes = [i, i, i, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_gemm_nvfp4.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_bf16.argtypes = [i, vp, i, i, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_mxfp8.argtypes = [i, vp, i, i, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_nvfp4.argtypes = [i, vp, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_grouped_scale_bytes.argtypes = [i, vp, i, i]
+            lib.tkg_grouped_scale_bytes.restype = ctypes.c_size_t
             lib.tkg_get_device_status.argtypes = [vp]
             lib.tkg_status_string.argtypes = [st]
             lib.tkg_status_string.restype = ctypes.c_char_p
@@ -114,6 +120,25 @@ def gemm_nvfp4_raw(m, n, k, A, B, sfa, sfb, ta, tb, D, alpha, stream) -> int:
     return load().tkg_gemm_nvfp4(m, n, k, A, B, sfa, sfb, ta, tb, D, ctypes.c_float(alpha), stream)
 
 
+def _sizes(m_sizes):
+    """Host int32 array of group sizes (kept alive by the caller's reference)."""
+    arr = (ctypes.c_int * len(m_sizes))(*[int(x) for x in m_sizes])
+    return arr, len(m_sizes)
+
+
+def gemm_grouped_bf16_raw(groups, m_sizes, n, k, A, B, D, alpha, stream) -> int:
+    return load().tkg_gemm_grouped_bf16(groups, m_sizes, n, k, A, B, D, ctypes.c_float(alpha), stream)
+
+
+def gemm_grouped_mxfp8_raw(groups, m_sizes, n, k, A, B, sfa, sfb, D, alpha, stream) -> int:
+    return load().tkg_gemm_grouped_mxfp8(groups, m_sizes, n, k, A, B, sfa, sfb, D, ctypes.c_float(alpha), stream)
+
+
+def gemm_grouped_nvfp4_raw(groups, m_sizes, n, k, A, B, sfa, sfb, ta, tb, D, alpha, stream) -> int:
+    return load().tkg_gemm_grouped_nvfp4(groups, m_sizes, n, k, A, B, sfa, sfb, ta, tb, D, ctypes.c_float(alpha),
+                                         stream)
+
+
 # ---------------------------------------------------------------- tensor helpers
 
 def gemm_bf16(A, B, D, alpha: float = 1.0, stream=None) -> None:
@@ -145,6 +170,38 @@ def gemm_nvfp4(A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, tb=None, stream=N
     n = B.shape[0]
     _check(gemm_nvfp4_raw(m, n, 2 * kh, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
                           alpha, _stream(stream)), "tkg_gemm_nvfp4")
+
+
+def gemm_grouped_bf16(m_sizes, A, B, D, alpha: float = 1.0, stream=None) -> None:
+    """Grouped: rows of A (sum(m_sizes) x k bf16) in consecutive groups, B (groups x n x k), D (sum x n)."""
+    arr, g = _sizes(m_sizes)
+    k = A.shape[-1]
+    n = B.shape[-2]
+    _check(gemm_grouped_bf16_raw(g, arr, n, k, _ptr(A), _ptr(B), _ptr(D), alpha, _stream(stream)),
+           "tkg_gemm_grouped_bf16")
+
+
+def gemm_grouped_mxfp8(m_sizes, A, B, sfa, sfb, D, alpha: float = 1.0, stream=None) -> None:
+    """Grouped MXFP8: per-group tiled SFA buffers back to back, SFB one tiled buffer per group."""
+    arr, g = _sizes(m_sizes)
+    k = A.shape[-1]
+    n = B.shape[-2]
+    _check(gemm_grouped_mxfp8_raw(g, arr, n, k, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(D), alpha,
+                                  _stream(stream)), "tkg_gemm_grouped_mxfp8")
+
+
+def gemm_grouped_nvfp4(m_sizes, A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, tb=None, stream=None) -> None:
+    """Grouped NVFP4: ta one FP32 (device) for A, tb one FP32 per group (device)."""
+    arr, g = _sizes(m_sizes)
+    k = 2 * A.shape[-1]
+    n = B.shape[-2]
+    _check(gemm_grouped_nvfp4_raw(g, arr, n, k, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb),
+                                  _ptr(D), alpha, _stream(stream)), "tkg_gemm_grouped_nvfp4")
+
+
+def grouped_scale_bytes(m_sizes, k: int, block: int) -> int:
+    arr, g = _sizes(m_sizes)
+    return int(load().tkg_grouped_scale_bytes(g, arr, k, block))
 
 
 def scale_bytes(rows: int, k: int, block: int) -> int:

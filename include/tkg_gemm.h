@@ -87,6 +87,40 @@ tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void *A, const void *B, con
                           const float *tensor_scale_a, const float *tensor_scale_b, void *D, float alpha,
                           cudaStream_t stream);
 
+/* Grouped GEMM, the mixture-of-experts form named as work in progress in
+ * "ThunderKittens 2.0 GPU Kernel优化" (section after Figure 1: grouped GEMM
+ * kernels under development).  The pages give no interface; this one keeps the
+ * plain GEMM's layouts per group.
+ *
+ * groups (1..128) groups of rows; m_sizes: HOST array of the groups' row
+ * counts (each >= 0, read during the call).  Group g owns the M_g = m_sizes[g]
+ * consecutive rows of A and D starting at row o_g = m_sizes[0] + ... +
+ * m_sizes[g-1], and multiplies them by its own n x k matrix B_g:
+ *   D[o_g + i][j] = bf16_rn(alpha_g * sum_k A[o_g + i][k] * B_g[j][k]).
+ * A: (sum M_g) x k, D: (sum M_g) x n, B: groups x n x k (B_g at row g * n),
+ * element types and per-format requirements as in the plain GEMMs; rows of D
+ * outside the groups' ranges are not written.
+ * Block scales: SFA holds each group's scales as its own tiled buffer of
+ * tkg_scale_bytes(M_g, k, bs) bytes, one after another (group g at the sum of
+ * the earlier groups' sizes; tkg_grouped_scale_bytes gives the total); SFB
+ * holds groups tiled buffers of tkg_scale_bytes(n, k, bs) bytes each.
+ * NVFP4: tensor_scale_a is NULL or one FP32 for all of A, tensor_scales_b NULL
+ * or one FP32 per group; alpha_g = fp32(fp32(alpha * tA) * tB[g]).
+ * Errors: groups < 1, m_sizes NULL or a negative size -> TKG_ERR_INVALID_ARG;
+ * groups > 128 -> TKG_ERR_UNSUPPORTED; otherwise as the plain GEMMs.  All
+ * groups empty or n == 0: nothing to do, TKG_OK. */
+tkg_status tkg_gemm_grouped_bf16(int groups, const int *m_sizes, int n, int k, const void *A, const void *B, void *D,
+                                 float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_grouped_mxfp8(int groups, const int *m_sizes, int n, int k, const void *A, const void *B,
+                                  const void *sfa, const void *sfb, void *D, float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_grouped_nvfp4(int groups, const int *m_sizes, int n, int k, const void *A, const void *B,
+                                  const void *sfa, const void *sfb, const float *tensor_scale_a,
+                                  const float *tensor_scales_b, void *D, float alpha, cudaStream_t stream);
+
+/* Bytes of a grouped SFA buffer: the sum over groups of
+ * tkg_scale_bytes(m_sizes[g], k, block).  0 for invalid arguments. */
+size_t tkg_grouped_scale_bytes(int groups, const int *m_sizes, int k, int block);
+
 /* BF16 GEMM that allocates nothing, for callers that cannot call cudaMalloc:
  * runtimes that reserve all of their device memory at start-up and forbid
  * allocation afterwards, or that run under a memory budget where an

@@ -175,6 +175,33 @@ def gemm_elems(fmt: str, A, B, sfa, sfb, alpha: float, ii, jj):
     return ref, S
 
 
+def gemm_grouped(fmt: str, m_sizes, A, B, sfa=None, sfb=None, alpha=1.0):
+    """Grouped GEMM by its definition: group g takes the m_sizes[g] rows of A
+    that follow the earlier groups' rows and multiplies them by B[g]^T.
+
+    A: (sum m_sizes, K or K/2); B: (groups, N, K or K/2); sfa: row-major scales
+    of all rows of A (sum m_sizes, ld_sf); sfb: (groups, N, ld_sf); alpha: one
+    value or one per group.  Returns (ref, S) of shape (sum m_sizes, N)."""
+    m_sizes = [int(x) for x in m_sizes]
+    groups = len(m_sizes)
+    assert B.shape[0] == groups
+    alphas = list(alpha) if np.ndim(alpha) else [float(alpha)] * groups
+    total = sum(m_sizes)
+    n = B.shape[1]
+    ref = np.zeros((total, n), dtype=np.float64)
+    S = np.zeros((total, n), dtype=np.float64)
+    row = 0
+    for g, mg in enumerate(m_sizes):
+        if mg > 0:
+            r, s = gemm(fmt, A[row:row + mg], B[g],
+                        None if sfa is None else sfa[row:row + mg], None if sfb is None else sfb[g],
+                        float(alphas[g]))
+            ref[row:row + mg] = r
+            S[row:row + mg] = s
+        row += mg
+    return ref, S
+
+
 def quant_mxfp8(X):
     """FP32 (rows, K) -> (E4M3 codes (rows, K), E8M0 scales (rows, ld_sf))."""
     X = np.ascontiguousarray(X, dtype=np.float32)

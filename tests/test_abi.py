@@ -70,3 +70,25 @@ def test_library_is_sm103a_only():
     # the build passes exactly one -gencode, for sm_103a
     from dense_block_scaled_gb300 import build
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_grouped_host_checks():
+    # argument checks that return before any device work
+    import ctypes
+    from dense_block_scaled_gb300 import tkg
+    sizes = lambda *v: (ctypes.c_int * len(v))(*v)
+    assert tkg.gemm_grouped_bf16_raw(0, sizes(1), 8, 8, None, None, None, 1.0, None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_grouped_bf16_raw(1, None, 8, 8, None, None, None, 1.0, None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_grouped_bf16_raw(2, sizes(3, -1), 8, 8, None, None, None, 1.0, None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_grouped_bf16_raw(129, sizes(*([1] * 129)), 8, 8, None, None, None, 1.0, None) == \
+        tkg.ERR_UNSUPPORTED
+    assert tkg.gemm_grouped_mxfp8_raw(2, sizes(0, 0), 8, 32, None, None, None, None, None, 1.0, None) == tkg.OK
+    assert tkg.gemm_grouped_nvfp4_raw(1, sizes(4), 0, 32, None, None, None, None, None, None, None, 1.0,
+                                      None) == tkg.OK
+
+
+def test_grouped_scale_bytes():
+    from dense_block_scaled_gb300 import tkg
+    sizes = [0, 1, 128, 129]
+    assert tkg.grouped_scale_bytes(sizes, 256, 16) == sum(tkg.scale_bytes(m, 256, 16) for m in sizes)
+    assert tkg.grouped_scale_bytes([2, -1], 256, 16) == 0

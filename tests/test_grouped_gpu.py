@@ -1,0 +1,150 @@
+"""Grouped GEMM (groups of rows of A, each against its own B) against the CPU
+oracle's grouped definition, through the C ABI: ragged and empty groups,
+group ends inside a 32-row store box, N tails, both CTA-group sizes, and the
+rows of D outside the groups left alone."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_block_scaled_gb300 import synth, tkg
+from helpers import assert_within_tolerance, bf16_to_f64, tiled_scales, to_dev
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["bf16", "mxfp8", "nvfp4"]
+
+
+@pytest.fixture(autouse=True)
+def _reset_options():
+    yield
+    tkg.set_option(tkg.OPT_CTA_GROUP, 0)
+
+
+class GroupedOperands:
+    """Seeded grouped operands: A (sum of sizes rows), B (groups x n x k); A is
+    quantised as one tensor, each B_g as its own tensor (NVFP4: one tensor
+    scale per group)."""
+
+    def __init__(self, fmt, sizes, n, k, seed, alpha=1.0):
+        self.fmt, self.sizes, self.n, self.k = fmt, list(sizes), n, k
+        groups, total = len(sizes), sum(sizes)
+        a, b = synth.gemm_inputs_f32(max(total, 1), groups * n, k, seed)
+        a = a[:total]
+        b = b.reshape(groups, n, k)
+        self.alphas = [alpha] * groups
+        self.sfa = self.sfb = None
+        self.ta, self.tb = None, None
+        if fmt == "bf16":
+            self.A = synth.bf16_codes(a)
+            self.B = synth.bf16_codes(b.reshape(groups * n, k)).reshape(groups, n, k)
+        elif fmt == "mxfp8":
+            self.A, self.sfa = oracle.quant_mxfp8(a)
+            qb = [oracle.quant_mxfp8(b[g]) for g in range(groups)]
+            self.B = np.stack([q for q, _ in qb])
+            self.sfb = np.stack([s for _, s in qb])
+        else:
+            self.A, self.sfa, self.ta = oracle.quant_nvfp4(a)
+            qb = [oracle.quant_nvfp4(b[g]) for g in range(groups)]
+            self.B = np.stack([q for q, _, _ in qb])
+            self.sfb = np.stack([s for _, s, _ in qb])
+            self.tb = [t for _, _, t in qb]
+            self.alphas = [oracle.alpha_eff(alpha, self.ta, t) for t in self.tb]
+
+    def reference(self):
+        return oracle.gemm_grouped(self.fmt, self.sizes, self.A, self.B, self.sfa, self.sfb, self.alphas)
+
+    def upload(self):
+        """Device tensors (A, B, sfa, sfb, ta, tb) in the grouped layouts."""
+        A, B = to_dev(self.A), to_dev(self.B)
+        if self.fmt == "bf16":
+            return A, B, None, None, None, None
+        kb = self.k // oracle.BLOCK[self.fmt]
+        parts, row = [], 0
+        for mg in self.sizes:
+            if mg:
+                parts.append(tiled_scales(self.sfa[row:row + mg], kb))
+            row += mg
+        sfa = to_dev(np.concatenate(parts) if parts else np.zeros(16, np.uint8))
+        sfb = to_dev(np.concatenate([tiled_scales(self.sfb[g], kb) for g in range(len(self.sizes))]))
+        ta = tb = None
+        if self.fmt == "nvfp4":
+            ta = torch.tensor([float(self.ta)], dtype=torch.float32, device="cuda")
+            tb = torch.tensor([float(t) for t in self.tb], dtype=torch.float32, device="cuda")
+        return A, B, sfa, sfb, ta, tb
+
+
+def run_grouped(fmt, sizes, dev, D, alpha=1.0):
+    A, B, sfa, sfb, ta, tb = dev
+    if fmt == "bf16":
+        tkg.gemm_grouped_bf16(sizes, A, B, D, alpha)
+    elif fmt == "mxfp8":
+        tkg.gemm_grouped_mxfp8(sizes, A, B, sfa, sfb, D, alpha)
+    else:
+        tkg.gemm_grouped_nvfp4(sizes, A, B, sfa, sfb, D, alpha, ta=ta, tb=tb)
+
+
+GUARD = 0x7F7F   # a BF16 NaN pattern no GEMM result takes
+
+
+def _check(fmt, sizes, n, k, seed, cta_group=0, alpha=1.0):
+    tkg.set_option(tkg.OPT_CTA_GROUP, cta_group)
+    ops = GroupedOperands(fmt, sizes, n, k, seed, alpha)
+    dev = ops.upload()
+    total = sum(sizes)
+    # D with 40 guard rows after the groups' rows: never written
+    Dfull = torch.full((total + 40, n), GUARD, dtype=torch.int16, device="cuda")
+    run_grouped(fmt, sizes, dev, Dfull.view(torch.bfloat16), alpha)
+    assert tkg.device_status() == tkg.OK
+    out = Dfull.cpu().numpy()
+    assert (out[total:] == GUARD).all(), "rows past the groups were written"
+    if total:
+        ref, S = ops.reference()
+        assert_within_tolerance(bf16_to_f64(out[:total].view(np.uint16)), ref, S,
+                                f"{fmt} sizes={sizes} n={n} k={k} cg={cta_group}")
+
+
+SIZES = [
+    [128, 256, 384],                 # whole tiles
+    [1, 0, 300, 129, 7],             # ragged, one empty group, ends inside store boxes
+    [0, 0, 5],                       # leading empty groups
+    [500],                           # one group
+]
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("sizes", SIZES, ids=lambda s: "-".join(map(str, s)))
+def test_grouped_matches_oracle(fmt, sizes, cta_group):
+    _check(fmt, sizes, 264, 512, seed=3000 + sum(sizes), cta_group=cta_group, alpha=0.5)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_many_groups(fmt):
+    # 40 groups of 0..200 rows, N a multiple of the tile, K with a ragged last stage
+    rng = np.random.default_rng(17)
+    sizes = [int(x) for x in rng.integers(0, 201, size=40)]
+    sizes[3] = 0
+    _check(fmt, sizes, 512, 1056 if fmt == "bf16" else 1088, seed=3100)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_all_empty_and_k0(fmt):
+    # every group empty: nothing is read or written
+    D = torch.full((8, 64), GUARD, dtype=torch.int16, device="cuda")
+    X = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    if fmt == "bf16":
+        tkg.gemm_grouped_bf16([0, 0], X, X.view(1, 64, 64), D.view(torch.bfloat16))
+    elif fmt == "mxfp8":
+        tkg.gemm_grouped_mxfp8([0, 0], X.view(64, 64), X.view(1, 64, 64), X, X, D.view(torch.bfloat16))
+    else:
+        tkg.gemm_grouped_nvfp4([0, 0], X.view(128, 32), X.view(2, 64, 32), X, X, D.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert (D.cpu().numpy() == GUARD).all()
+    # K = 0: the groups' rows of D become zero, the rest untouched
+    A = torch.zeros((6, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((2, 64, 0), dtype=torch.bfloat16, device="cuda")
+    tkg.gemm_grouped_bf16([2, 4], A, B, D.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    out = D.cpu().numpy()
+    assert (out[:6] == 0).all() and (out[6:] == GUARD).all()

@@ -432,3 +432,37 @@ def test_gemm_elems_equal_rows(fmt):
     assert np.array_equal(r2, ref[ii, jj]) and np.array_equal(s2, S[ii, jj])
     r3, s3 = oracle.gemm(fmt, A, B, sfa, sfb, 1.5, rows=(5, 7))
     assert np.array_equal(r3, ref[5:12]) and np.array_equal(s3, S[5:12])
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+def test_gemm_grouped_bruteforce_fraction(fmt):
+    # grouped GEMM: each group's rows against its own B, per-group alpha;
+    # checked against the exact rational product of the group's slice
+    sizes = [3, 0, 5, 1]
+    n, k = 6, 64
+    lo, hi = {"bf16": (0, 1), "mxfp8": (125, 130), "nvfp4": (0x20, 0x50)}[fmt]
+    A, _, sfa, _ = _rand_operands(fmt, sum(sizes), 1, k, seed=31, sf_lo=lo, sf_hi=hi)
+    Bs, sfbs = [], []
+    for g in range(len(sizes)):
+        _, Bg, _, sfbg = _rand_operands(fmt, 1, n, k, seed=40 + g, sf_lo=lo, sf_hi=hi)
+        Bs.append(Bg)
+        sfbs.append(sfbg)
+    B = np.stack(Bs)
+    sfb = None if fmt == "bf16" else np.stack(sfbs)
+    alphas = [0.5, 2.0, -1.0, 0.25]
+    ref, S = oracle.gemm_grouped(fmt, sizes, A, B, sfa, sfb, alphas)
+    assert ref.shape == (sum(sizes), n)
+    row = 0
+    for g, mg in enumerate(sizes):
+        if mg == 0:
+            continue
+        sl = slice(row, row + mg)
+        eref, eS = _exact_gemm(fmt, A[sl], B[g], None if sfa is None else sfa[sl],
+                               None if sfb is None else sfb[g], alphas[g])
+        for i in range(mg):
+            for j in range(n):
+                if fmt == "bf16":
+                    assert abs(Fraction(ref[row + i, j]) - eref[i][j]) <= Fraction(2) ** -52 * eS[i][j]
+                else:
+                    assert Fraction(ref[row + i, j]) == eref[i][j], (g, i, j)
+        row += mg
