@@ -28,6 +28,7 @@ EXPORTS = [
     "tkg_scale_bytes", "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
     "tkg_set_option", "tkg_get_option", "tkg_gemm_bf16_noalloc",
     "tkg_gemm_grouped_bf16", "tkg_gemm_grouped_mxfp8", "tkg_gemm_grouped_nvfp4", "tkg_grouped_scale_bytes",
+    "tkg_gemm_bf16_from_host",
 ]
 
 _lock = threading.Lock()
@@ -58,6 +59,7 @@ def load() -> ctypes.CDLL:
             lib.tkg_gemm_grouped_nvfp4.argtypes = [i, vp, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_grouped_scale_bytes.argtypes = [i, vp, i, i]
             lib.tkg_grouped_scale_bytes.restype = ctypes.c_size_t
+            lib.tkg_gemm_bf16_from_host.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_get_device_status.argtypes = [vp]
             lib.tkg_status_string.argtypes = [st]
             lib.tkg_status_string.restype = ctypes.c_char_p
@@ -197,6 +199,15 @@ def gemm_grouped_nvfp4(m_sizes, A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, 
     n = B.shape[-2]
     _check(gemm_grouped_nvfp4_raw(g, arr, n, k, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb),
                                   _ptr(D), alpha, _stream(stream)), "tkg_gemm_grouped_nvfp4")
+
+
+def gemm_bf16_from_host(A_host, B_host, D_host, A_dev, B_dev, D_dev, alpha: float = 1.0, stream=None) -> None:
+    """D_host = alpha * A_host @ B_host^T with host (pinned) operands; *_dev are device staging buffers."""
+    m, k = A_host.shape
+    n = B_host.shape[0]
+    _check(load().tkg_gemm_bf16_from_host(m, n, k, _ptr(A_host), _ptr(B_host), _ptr(D_host), _ptr(A_dev),
+                                          _ptr(B_dev), _ptr(D_dev), ctypes.c_float(alpha), _stream(stream)),
+           "tkg_gemm_bf16_from_host")
 
 
 def grouped_scale_bytes(m_sizes, k: int, block: int) -> int:

@@ -121,6 +121,22 @@ tkg_status tkg_gemm_grouped_nvfp4(int groups, const int *m_sizes, int n, int k, 
  * tkg_scale_bytes(m_sizes[g], k, block).  0 for invalid arguments. */
 size_t tkg_grouped_scale_bytes(int groups, const int *m_sizes, int k, int block);
 
+/* BF16 GEMM on operands in HOST memory (the same product as tkg_gemm_bf16;
+ * no counterpart on the pages, which time device-resident GEMMs only).
+ * A_host (m x k), B_host (n x k): bfloat16, row-major, read; D_host (m x n):
+ * written.  A_dev, B_dev, D_dev: caller-owned device buffers of the same
+ * sizes used as staging (16-byte aligned); their contents afterwards are
+ * unspecified except D_dev = D.  The call copies B, then A in bands of rows on
+ * one internal stream, runs each band's GEMM on `stream` as its rows arrive,
+ * and copies each band of D back on a second internal stream, so the copies
+ * overlap the GEMM; host buffers must be page-locked (cudaHostAlloc /
+ * cudaHostRegister) for that overlap.  Asynchronous: everything starts after
+ * the work already queued on `stream`, and work queued on `stream` afterwards
+ * starts after D_host is written.  Concurrent calls from several threads are
+ * serialised while they enqueue.  Checks and errors as tkg_gemm_bf16. */
+tkg_status tkg_gemm_bf16_from_host(int m, int n, int k, const void *A_host, const void *B_host, void *D_host,
+                                   void *A_dev, void *B_dev, void *D_dev, float alpha, cudaStream_t stream);
+
 /* BF16 GEMM that allocates nothing, for callers that cannot call cudaMalloc:
  * runtimes that reserve all of their device memory at start-up and forbid
  * allocation afterwards, or that run under a memory budget where an
