@@ -8,8 +8,10 @@ sampled during the run.
 
 Headline: BF16 D = A.B^T at M=N=K=16384 (the largest point of the BF16 square
 sweep), TFLOP/s = 2MNK / t.  The same JSON line carries the rest of the BF16
-sweep and the MXFP8 / NVFP4 16384^3 GEMMs (operands quantised on the GPU by the
-library's own quantisers), each with its roofline fraction.
+sweep (512 .. 8192), the MXFP8 / NVFP4 GEMMs at 4096, 8192 and 16384 (operands
+quantised on the GPU by the library's own quantisers), the skinny N=K=8192 shapes,
+the quantisers, a grouped GEMM and the end-to-end host-buffer GEMM, each with
+its roofline fraction.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -44,7 +46,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--size", type=int, default=16384, help="headline M=N=K")
     ap.add_argument("--formats", default="bf16,mxfp8,nvfp4")
-    ap.add_argument("--sweep", default="2048,4096,8192", help="extra BF16 sizes reported beside the headline")
+    ap.add_argument("--sweep", default="512,2048,4096,8192", help="extra BF16 sizes reported beside the headline")
+    ap.add_argument("--sweep-scaled", default="4096,8192", help="extra MXFP8 / NVFP4 sizes reported beside 16384")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-rows", type=int, default=768, help="rows of the oracle's CPU-baseline sample")
     ap.add_argument("--head-format", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
@@ -520,7 +523,7 @@ def run_ours(args):
                 "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
                 "measured_peak_tflops": peak_meas, "input_groups": w.groups}
 
-    by_format, sweep, skinny, quant, grouped = {}, {}, {}, {}, {}
+    by_format, sweep, sweep_scaled, skinny, quant, grouped = {}, {}, {}, {}, {}, {}
     e2e = None
     if rank == 0:
         by_format[hf] = fmt_entry(head, t_head)
@@ -544,6 +547,14 @@ def run_ours(args):
                              "us_graph": tg * 1e6, "tflops_graph": w.flop / tg / 1e12}
             del w
             torch.cuda.empty_cache()
+        for fmt in ("mxfp8", "nvfp4"):
+            for s in [int(x) for x in args.sweep_scaled.split(",") if x]:
+                w = Workload(fmt, s, SEEDS[fmt], l2, torch, tkg, synth)
+                t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+                sweep_scaled[f"{fmt} {s}"] = {"tflops": w.flop / t / 1e12, "us": t * 1e6, "input_groups": w.groups,
+                                              "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS[fmt]}
+                del w
+                torch.cuda.empty_cache()
         for fmt in ("bf16", "nvfp4"):
             for mm in [int(x) for x in args.skinny.split(",") if x]:
                 w = Workload(fmt, 8192, 1004, l2, torch, tkg, synth, mnk=(mm, 8192, 8192))
@@ -595,6 +606,7 @@ def run_ours(args):
             "clocks": clk,
             "formats": by_format,
             "sweep_bf16": sweep,
+            "sweep_scaled": sweep_scaled,
             "skinny": skinny,
             "quantize": quant,
             "grouped": grouped,

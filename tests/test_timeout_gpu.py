@@ -41,3 +41,26 @@ def test_stalled_wait_times_out_and_recovers(fmt, cta_group, split):
     tkg.set_option(tkg.OPT_CTA_GROUP, 0)
     tkg.set_option(tkg.OPT_SPLIT_K, 0)
     torch.cuda.synchronize()
+
+
+def test_grouped_stall_times_out_and_recovers():
+    # the grouped instantiation shares the bounded waits
+    from test_grouped_gpu import GroupedOperands, run_grouped
+    sizes = [300, 0, 257]
+    ops = GroupedOperands("mxfp8", sizes, 264, 512, seed=78)
+    dev = ops.upload()
+    D = torch.empty((sum(sizes), 264), dtype=torch.bfloat16, device="cuda")
+    try:
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 100)
+        tkg.set_option(tkg.OPT_INJECT_STALL, 1)
+        t0 = time.time()
+        run_grouped("mxfp8", sizes, dev, D)
+        assert tkg.device_status() == tkg.ERR_TIMEOUT
+        assert time.time() - t0 < 10.0
+    finally:
+        tkg.set_option(tkg.OPT_INJECT_STALL, 0)
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 0)
+    run_grouped("mxfp8", sizes, dev, D)
+    assert tkg.device_status() == tkg.OK
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, "grouped after recovery")
