@@ -436,6 +436,21 @@ def l2_description(groups, mode):
     return "inputs larger than 3x L2, no rotation needed" if groups == 1 else f"{groups} rotated input groups"
 
 
+def max_over_ranks(t, dist, torch, device):
+    """The job's time: the slowest rank's (each rank times the same number of
+    steps of its own replica)."""
+    if dist is None:
+        return t
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(world, units_per_rank, t_max):
+    """Whole-job throughput: the units every rank processed, over the job's time."""
+    return world * units_per_rank / t_max
+
+
 def run_reference(args):
     """CPU oracle on the host cores: each step = a sample of output elements."""
     rank = int(os.environ.get("RANK", "0"))
@@ -507,13 +522,8 @@ def run_ours(args):
     t_head = time_launches(head, args.steps, args.warmup, torch, tkg, dist, args.l2, flush_buf)
     clk = clocks.stop()
 
-    # max over ranks
-    t_max = t_head
-    if dist is not None:
-        tt = torch.tensor([t_head], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = world * head.flop / t_max / 1e12
+    t_max = max_over_ranks(t_head, dist, torch, "cuda")
+    value = job_value(world, head.flop, t_max) / 1e12
     achieved = head.flop / t_head / 1e12
 
     def fmt_entry(w, t):
