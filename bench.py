@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--formats", default="bf16,mxfp8,nvfp4")
     ap.add_argument("--sweep", default="512,2048,4096,8192", help="extra BF16 sizes reported beside the headline")
     ap.add_argument("--sweep-scaled", default="4096,8192", help="extra MXFP8 / NVFP4 sizes reported beside 16384")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=768, help="rows of the oracle's CPU-baseline sample")
     ap.add_argument("--head-format", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
                     help="format of the first (timed, clock-sampled) workload; profiling runs pick it")
@@ -396,7 +396,7 @@ def e2e_seconds(w, steps, torch, tkg):
         w.launch(0, tkg)
         Dh.copy_(w.D[0], non_blocking=True)
 
-    for _ in range(2):
+    for _ in range(3):   # warm-up steps, as for the device timing
         step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)

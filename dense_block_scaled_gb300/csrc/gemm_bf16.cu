@@ -16,6 +16,8 @@ tkg_status launch_bf16(const Problem& pr, cudaStream_t s) {
   if (split == 2) return launch_splitk<FMT_BF16, 2, 6>(pr, s);
   if (split == 3) return launch_splitk<FMT_BF16, 3, 6>(pr, s);
   if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_BF16, 2, 256, 1, 2>(pr, s);
+  if (cg != 1 && option(TKG_OPT_ACC_STAGES) != 1 && use_dual_bf16(pr))
+    return launch_sched<FMT_BF16, 2, 512, 4, 1>(pr, s);
   if (cg == 1) return launch_sched<FMT_BF16, 1, 256, 4, 2>(pr, s);
   if (option(TKG_OPT_ACC_STAGES) == 1) return launch_sched<FMT_BF16, 2, 256, 6, 1>(pr, s);
   return launch_sched<FMT_BF16, 2, 256, 6, 2>(pr, s);

@@ -156,6 +156,12 @@ struct GemmConfig {
   static constexpr int kCtaM = 128;                 // accumulator rows per CTA
   static constexpr int kMmaM = 128 * CG;
   static constexpr int kBRows = BN / CG;            // B rows loaded by each CTA
+  // Dual accumulate (BN = 512, BF16): two N=256 MMAs per K step share the A
+  // tile ("ThunderKittens 2.0" §二 2.2); each CTA loads two 128-row boxes of B,
+  // one per half of the 512-column tile
+  static constexpr bool kDual = BN == 512;
+  static constexpr int kBBox = kDual ? kBRows / 2 : kBRows;
+  static constexpr int kMmaN = kDual ? 256 : BN;
   static constexpr int kRowBytes = 128;             // K bytes per stage row
   static constexpr int kABytes = kCtaM * kRowBytes;
   static constexpr int kBBytes = kBRows * kRowBytes;
@@ -192,11 +198,12 @@ struct GemmConfig {
   static constexpr int kTmemCols = 512;
   static_assert(!kScaled || kRegions >= 2, "tensor memory overflow");
   static_assert(ACC * kAccCols <= kTmemCols, "tensor memory overflow");
-  static_assert(BN == 128 || BN == 256, "B tiles must cover whole 128-row scale blocks");
+  static_assert(BN == 128 || BN == 256 || (BN == 512 && !kScaled && ACC == 1 && CG == 2),
+                "B tiles must cover whole 128-row scale blocks; dual accumulate is BF16 pairs only");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static constexpr uint32_t kIdescBase =
-      FMT == FMT_BF16 ? idesc_f16(kMmaM, BN)
-                      : idesc_bs(kMmaM, BN, FMT == FMT_NVFP4 ? 1u : 0u, FMT == FMT_MXFP8 ? 1u : 0u, 0u, 0u);
+      FMT == FMT_BF16 ? idesc_f16(kMmaM, kMmaN)
+                      : idesc_bs(kMmaM, kMmaN, FMT == FMT_NVFP4 ? 1u : 0u, FMT == FMT_MXFP8 ? 1u : 0u, 0u, 0u);
 };
 
 struct Ctl {
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(384, 1)
       const int local_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
       tc.a_row = gt.row0[g] + local_row;
       tc.row_limit = gt.row0[g] + gt.rows[g];
-      tc.b_row = g * p.n + tc.nb * BN + int(rank) * C::kBRows;
+      tc.b_row = g * p.n + tc.nb * BN + int(rank) * C::kBBox;
       tc.sfa_block = gt.sfa_block0[g] + local_row / 128;
       tc.sfb_block0 = g * gt.n_blocks + (tc.nb * BN) / 128;
       tc.group = g;
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(384, 1)
       tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, tc.mb, tc.nb);
       tc.a_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
       tc.row_limit = p.m;
-      tc.b_row = tc.nb * BN + int(rank) * C::kBRows;
+      tc.b_row = tc.nb * BN + int(rank) * C::kBBox;
       tc.sfa_block = tc.a_row / 128;
       tc.sfb_block0 = (tc.nb * BN) / 128;
       tc.group = 0;
@@ -447,6 +454,8 @@ __global__ void __launch_bounds__(384, 1)
           const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);   // TMA x coordinate (elements)
           ptx::tma_load_2d<CG>(stage_a(stage), &tmA, kx, a_row, fb, pol_a);
           ptx::tma_load_2d<CG>(stage_b(stage), &tmB, kx, b_row, fb, pol_b);
+          if constexpr (C::kDual)   // second half of the 512-column tile
+            ptx::tma_load_2d<CG>(stage_b(stage) + uint32_t(C::kBBytes / 2), &tmB, kx, b_row + BN / 2, fb, pol_b);
           if constexpr (C::kScaled) {
             const int atom0 = ks * T::kSfAtoms;
             // SFA: this CTA's 128 rows = scale block (a_row / 128)
@@ -518,6 +527,10 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
             if constexpr (FMT == FMT_BF16) {
               ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, accum);
+              if constexpr (C::kDual) {
+                const uint64_t bdesc1 = sdesc_sw128(stage_b(stage) + uint32_t(C::kBBytes / 2));
+                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, C::kIdescBase, accum);
+              }
             } else {
               // scales -> tensor memory from this thread, right before the MMAs that
               // read them: one region per stage (MXFP8: MMA j reads byte j of each
@@ -598,10 +611,9 @@ __global__ void __launch_bounds__(384, 1)
   else if (warp >= 4) {
     const int e = warp - 4;
     const int q = warp & 3;              // accumulator lane quadrant this warp may read
-    const int h = e >> 2;                // column half: [0, 128) or [128, BN)
-    constexpr int kChunksLo = 4;
-    constexpr int kChunksHi = BN / 32 - 4;
-    const int nch = h == 0 ? kChunksLo : kChunksHi;
+    const int h = e >> 2;                // column half of the tile: [0, BN/2) or [BN/2, BN)
+    constexpr int kWarpChunks = BN / 64;               // 32-column accumulator chunks per warp
+    constexpr int kPasses = (kWarpChunks + 3) / 4;     // four chunks (128 registers) per pass
     const uint32_t my_buf0 = epi_base + uint32_t(e * C::kEpiBufs * C::kEpiBufBytes);
     const uint32_t acce_lead0 = (CG == 2) ? ptx::map_to_rank(acce_bar(0), 0) : acce_bar(0);
     float alpha0 = p.alpha;
@@ -621,88 +633,96 @@ __global__ void __launch_bounds__(384, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t v[4][32];
-      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * 128);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c < nch) ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v[c]);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        // Accumulator buffer free.  The loads above have completed (wait::ld),
-        // so only the signal has to reach the MMA issuer: leader warps arrive
-        // on it directly; each follower warp sends a 16-byte async copy whose
-        // completion the leader's warp of the same index expects on the same
-        // barrier.  (A cluster-scope release arrive costs a cluster-wide fence.)
-        if (CG == 1) {
-          ptx::mbar_arrive(acce_bar(acc));
-        } else if (leader) {
-          ptx::mbar_arrive_expect_tx(acce_bar(acc), 16u);
-        } else {
-          ptx::bulk_copy_to_cluster(ptx::map_to_rank(epi_sig_slot(e), 0), epi_sig_slot(e), 16u, acce_lead0 + 8u * acc);
-        }
-      }
-      if (++acc == ACC) {
-        acc = 0;
-        accph ^= 1u;
-      }
       const int row0 = tc.a_row + q * 32;
-      const int col0 = tc.nb * BN + h * 128;
       // a 32-row box that crosses the end of a group (grouped GEMM) is stored
       // row by row so that the next group's rows are left alone
       const bool masked = GROUPED && row0 + 32 > tc.row_limit;
-      if (masked) {
-        if constexpr (GROUPED) {
-          const int r = row0 + lane;
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (c >= nch) break;
+      for (int pass = 0; pass < kPasses; ++pass) {
+        const int nch = kWarpChunks - 4 * pass < 4 ? kWarpChunks - 4 * pass : 4;
+        uint32_t v[4][32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t w[4];
+        for (int c = 0; c < 4; ++c)
+          if (c < nch) ptx::tmem_ld_32x32b_x32(tbase + uint32_t(pass * 128 + c * 32), v[c]);
+        ptx::tmem_ld_wait();
+        if (pass == kPasses - 1) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            // Accumulator buffer free.  The loads above have completed (wait::ld),
+            // so only the signal has to reach the MMA issuer: leader warps arrive
+            // on it directly; each follower warp sends a 16-byte async copy whose
+            // completion the leader's warp of the same index expects on the same
+            // barrier.  (A cluster-scope release arrive costs a cluster-wide fence.)
+            if (CG == 1) {
+              ptx::mbar_arrive(acce_bar(acc));
+            } else if (leader) {
+              ptx::mbar_arrive_expect_tx(acce_bar(acc), 16u);
+            } else {
+              ptx::bulk_copy_to_cluster(ptx::map_to_rank(epi_sig_slot(e), 0), epi_sig_slot(e), 16u,
+                                        acce_lead0 + 8u * acc);
+            }
+          }
+          if (++acc == ACC) {
+            acc = 0;
+            accph ^= 1u;
+          }
+        }
+        const int col0 = tc.nb * BN + h * (BN / 2) + pass * 128;
+        if (masked) {
+          if constexpr (GROUPED) {
+            const int r = row0 + lane;
 #pragma unroll
-              for (int x = 0; x < 4; ++x)
-                w[x] = ptx::pack_bf16x2(__uint_as_float(v[c][8 * j + 2 * x]) * alpha,
-                                        __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha);
-              const int col = col0 + c * 32 + j * 8;
-              if (r < tc.row_limit && col < p.n) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(gt.d) + size_t(r) * size_t(gt.ldd) + col);
-                *dst = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < 4; ++c) {
+              if (c >= nch) break;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                  w[x] = ptx::pack_bf16x2(__uint_as_float(v[c][8 * j + 2 * x]) * alpha,
+                                          __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha);
+                const int col = col0 + c * 32 + j * 8;
+                if (r < tc.row_limit && col < p.n) {
+                  uint4* dst =
+                      reinterpret_cast<uint4*>(static_cast<uint16_t*>(gt.d) + size_t(r) * size_t(gt.ldd) + col);
+                  *dst = make_uint4(w[0], w[1], w[2], w[3]);
+                }
               }
             }
           }
         }
-      }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c >= nch || masked) break;
-        const uint32_t buf = my_buf0 + uint32_t((C::kEpiBufs == 2 ? (c & 1) : 0) * C::kEpiBufBytes);
-        if (lane == 0) {
-          if (C::kEpiBufs == 2)
-            ptx::bulk_wait_group_read<1>();
-          else
-            ptx::bulk_wait_group_read<0>();
-        }
-        __syncwarp();
-        const uint32_t row_addr = buf + uint32_t(lane * 64);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t w[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float lo = __uint_as_float(v[c][8 * j + 2 * x]) * alpha;
-            const float hi = __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha;
-            w[x] = ptx::pack_bf16x2(lo, hi);
+        for (int c = 0; c < 4; ++c) {
+          if (c >= nch || masked) break;
+          const uint32_t buf = my_buf0 + uint32_t((C::kEpiBufs == 2 ? (c & 1) : 0) * C::kEpiBufBytes);
+          if (lane == 0) {
+            if (C::kEpiBufs == 2)
+              ptx::bulk_wait_group_read<1>();
+            else
+              ptx::bulk_wait_group_read<0>();
           }
-          const uint32_t chunk = uint32_t(j) ^ ((uint32_t(lane) >> 1) & 3u);   // 64-byte swizzle
-          ptx::st_shared_v4(row_addr + chunk * 16u, w[0], w[1], w[2], w[3]);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_2d(&tmD, buf, col0 + c * 32, row0);
-          ptx::bulk_commit_group();
+          __syncwarp();
+          const uint32_t row_addr = buf + uint32_t(lane * 64);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float lo = __uint_as_float(v[c][8 * j + 2 * x]) * alpha;
+              const float hi = __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha;
+              w[x] = ptx::pack_bf16x2(lo, hi);
+            }
+            const uint32_t chunk = uint32_t(j) ^ ((uint32_t(lane) >> 1) & 3u);   // 64-byte swizzle
+            ptx::st_shared_v4(row_addr + chunk * 16u, w[0], w[1], w[2], w[3]);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmD, buf, col0 + c * 32, row0);
+            ptx::bulk_commit_group();
+          }
         }
       }
       int nt = 0;

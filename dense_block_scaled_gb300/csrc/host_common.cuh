@@ -34,22 +34,43 @@ tkg_status device_status_word(unsigned int** out);   // lazily allocated per dev
 tkg_status device_sm_count(int* out);
 tkg_status device_l2_bytes(int* out);
 
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
 // M-blocks per raster band: as many as let the band's A panels (rows x K
 // bytes each) fill about a quarter of L2, between 4 and 32 (measured best at
 // 16384^3 on GB300: BF16 4-8, MXFP8 8, NVFP4 16 bands; at half of L2 NVFP4
-// loses 9%).
-inline int raster_group(int block_rows, int k, int fmt, int tiles_m) {
+// loses 9%).  With dual accumulate the B panels are twice as wide, and bands
+// three times as tall (capped at 12) measured best (BF16 16384^3: 12).
+inline int raster_group(int block_rows, int k, int fmt, int tiles_m, bool dual = false) {
   const int forced = option(TKG_OPT_RASTER_GROUP);
   if (forced > 0) return forced < tiles_m ? forced : (tiles_m > 0 ? tiles_m : 1);
   int l2 = 0;
   if (device_l2_bytes(&l2) != TKG_OK || l2 <= 0) l2 = 96 << 20;
   const double bytes_per_elem = fmt == 0 ? 2.0 : (fmt == 1 ? 1.0 : 0.5);
   const double panel = double(block_rows) * double(k) * bytes_per_elem;
-  int g = int(0.25 * double(l2) / (panel > 1.0 ? panel : 1.0) + 0.5);
+  int g = int((dual ? 0.75 : 0.25) * double(l2) / (panel > 1.0 ? panel : 1.0) + 0.5);
   if (g < 4) g = 4;
-  if (g > 32) g = 32;
+  if (g > (dual ? 12 : 32)) g = dual ? 12 : 32;
   if (g > tiles_m) g = tiles_m > 0 ? tiles_m : 1;
   return g;
+}
+
+// BF16 dual accumulate (256 x 512 pair tiles) unless the wider tiles fill the
+// waves of CTA pairs clearly worse than 256 x 256 tiles do (2048-row bands of
+// 16384^2: 3.4 waves against 6.7; 2048^3: half a wave); TKG_OPT_BF16_TILE_N
+// forces 256 or 512.
+inline bool use_dual_bf16(const Problem& pr) {
+  const int forced = option(TKG_OPT_BF16_TILE_N);
+  if (forced == 512) return true;
+  if (forced == 256) return false;
+  int sms = 0;
+  if (device_sm_count(&sms) != TKG_OK || sms < 2) return false;
+  const double pairs = double(sms / 2);
+  auto filled = [&](int bn) {
+    const double tiles = double(ceil_div(pr.m, 256)) * double(ceil_div(pr.n, bn));
+    return tiles / (double((long long)((tiles + pairs - 1.0) / pairs)) * pairs);
+  };
+  return filled(512) >= filled(256) - 0.02;
 }
 
 // ---- tensor maps (tkg_api.cu)
@@ -59,7 +80,6 @@ tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
                      uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                      uint32_t box2);
 
-inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Launch one instantiation of the persistent GEMM (or, with GROUPED, of the
 // grouped GEMM over pr.groups groups of rows).
@@ -129,7 +149,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   tkg_status st;
   if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBBox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
@@ -164,7 +184,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
-  p.raster_group = raster_group(C::kMmaM, pr.k, FMT, max_tiles_m);
+  p.raster_group = raster_group(C::kMmaM, pr.k, FMT, max_tiles_m, C::kDual);
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;

@@ -22,6 +22,7 @@ OPT_CTA_GROUP, OPT_SINGLE_STAGE, OPT_TIMEOUT_MS, OPT_INJECT_STALL, OPT_MAX_CLUST
 OPT_SCHEDULER = 7
 OPT_SPLIT_K = 8
 OPT_RASTER_GROUP = 9
+OPT_BF16_TILE_N = 10
 
 EXPORTS = [
     "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",

@@ -17,7 +17,7 @@ FMTS = ["bf16", "mxfp8", "nvfp4"]
 
 ALL_OPTIONS = (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
                tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER, tkg.OPT_SPLIT_K,
-               tkg.OPT_RASTER_GROUP)
+               tkg.OPT_RASTER_GROUP, tkg.OPT_BF16_TILE_N)
 
 
 @pytest.fixture(autouse=True)
@@ -51,6 +51,15 @@ def test_gemm_matches_oracle(fmt, shape, cta_group):
     # persistent kernel (split-K disabled)
     m, n, k = shape
     _check(fmt, m, n, k, seed=1000 + m + n + k, alpha=1.0, cta_group=cta_group, split=1)
+
+
+@pytest.mark.parametrize("shape", SHAPES + [(1024, 1536, 768), (600, 1000, 4000)])
+def test_bf16_dual_accumulate_matches_oracle(shape):
+    # 256 x 512 pair tiles: two N=256 MMAs per K step into the two halves of
+    # tensor memory, sharing the A tile
+    m, n, k = shape
+    tkg.set_option(tkg.OPT_BF16_TILE_N, 512)
+    _check("bf16", m, n, k, seed=1700 + m + n + k, alpha=0.5, split=1)
 
 
 SPLIT_SHAPES = [(512, 512, 512), (300, 264, 320), (16, 1024, 2048), (5, 136, 4000), (128, 256, 96), (33, 256, 512)]
