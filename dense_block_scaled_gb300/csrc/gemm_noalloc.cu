@@ -115,6 +115,7 @@ extern "C" tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void* A, 
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = 0;
   p.raster_group = 8;
+  p.wave = 0;
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;

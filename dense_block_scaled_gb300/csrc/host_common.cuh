@@ -232,6 +232,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if (SCHED == SCHED_CLC) clusters = p.num_tiles;
   cfg.gridDim = dim3(clusters * CG, 1, 1);
 
+  p.wave = max_clusters;   // the serpentine K order flips every wave of resident clusters
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p, gt);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -296,6 +297,7 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
+  p.wave = 0;
   p.raster_group = raster_group(C::BM, pr.k, FMT, p.tiles_m);
 
   cudaLaunchConfig_t cfg = {};

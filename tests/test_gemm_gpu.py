@@ -113,6 +113,7 @@ def test_launch_control_equals_static_schedule(fmt):
 def test_single_stage_equals_deep_pipeline(fmt):
     # pipeline depth 1 and the deep ring must give identical bits ("异步Tensor Core原理与实战", §5.2)
     m, n, k = 384, 512, 1024
+    tkg.set_option(tkg.OPT_SPLIT_K, 1)   # the persistent kernel, whose ring depth is under test
     ops = Operands(fmt, m, n, k, seed=11)
     dev = ops.upload()
     D_deep = run_gemm(fmt, dev, m, n, k, 1.0)
