@@ -290,9 +290,14 @@ def test_full_size_sampled(fmt, size):
     dev = ops.upload()
     D = run_gemm(fmt, dev, m, n, k, 1.0)
     assert tkg.device_status() == tkg.OK
+    # 2^16 random outputs, plus every output of the first and last rows and
+    # columns and of the rows / columns on tile seams (128, 256, 512)
     rng = np.random.default_rng(size)
-    ii = np.concatenate([rng.integers(0, m, 3000), [0, m - 1, m - 1, 0, 255, 256, 127, 128]])
-    jj = np.concatenate([rng.integers(0, n, 3000), [0, n - 1, 0, n - 1, 256, 255, 128, 127]])
+    edge_r = np.array([0, m - 1, 127, 128, 255, 256, 511, 512])
+    edge_c = np.array([0, n - 1, 127, 128, 255, 256, 511, 512])
+    cols, rows = np.arange(n), np.arange(m)
+    ii = np.concatenate([rng.integers(0, m, 1 << 16), np.repeat(edge_r, n), np.tile(rows, edge_c.size)])
+    jj = np.concatenate([rng.integers(0, n, 1 << 16), np.tile(cols, edge_r.size), np.repeat(edge_c, m)])
     ref, S = ops.reference_elems(ii, jj)
     got = bf16_to_f64(D[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()])
     assert_within_tolerance(got, ref, S, f"{fmt} {size}^3 sampled")
