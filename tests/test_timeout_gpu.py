@@ -64,3 +64,28 @@ def test_grouped_stall_times_out_and_recovers():
     assert tkg.device_status() == tkg.OK
     ref, S = ops.reference()
     assert_within_tolerance(bf16_to_f64(D), ref, S, "grouped after recovery")
+
+
+def test_dual_accumulate_stall_times_out_and_recovers():
+    # the 256 x 512 BF16 tile variant shares the bounded waits
+    m, n, k = 512, 1024, 1024
+    ops = Operands("bf16", m, n, k, seed=79)
+    dev = ops.upload()
+    tkg.set_option(tkg.OPT_BF16_TILE_N, 512)
+    tkg.set_option(tkg.OPT_SPLIT_K, 1)
+    try:
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 100)
+        tkg.set_option(tkg.OPT_INJECT_STALL, 1)
+        t0 = time.time()
+        run_gemm("bf16", dev, m, n, k, 1.0)
+        assert tkg.device_status() == tkg.ERR_TIMEOUT
+        assert time.time() - t0 < 10.0
+    finally:
+        tkg.set_option(tkg.OPT_INJECT_STALL, 0)
+        tkg.set_option(tkg.OPT_TIMEOUT_MS, 0)
+    D = run_gemm("bf16", dev, m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    tkg.set_option(tkg.OPT_BF16_TILE_N, 0)
+    tkg.set_option(tkg.OPT_SPLIT_K, 0)
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, "dual after recovery")
