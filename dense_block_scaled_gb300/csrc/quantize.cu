@@ -74,54 +74,59 @@ __device__ __forceinline__ WarpRange warp_range(long long passes, int unroll) {
   return {p0, p0 + per < passes ? p0 + per : passes};
 }
 
-// MXFP8: a warp pass covers 512 contiguous bytes of X (lane l loads the float4
-// at 16*l), four 32-element blocks; the block amax meets over 8 lanes.  Four
-// passes per loop trip, all loads issued before any arithmetic.
+// MXFP8: each lane takes 8 consecutive elements (two adjacent float4), so a
+// 32-element block spans 4 lanes and a warp pass covers 8 blocks (1 KB of X);
+// four passes per loop trip, all loads issued before any arithmetic.  Fewer
+// shuffles and conversions per element than 4 elements a lane matter once the
+// power cap lowers the clock (the kernel is then issue-bound).
 constexpr int kMxUnroll = 4;
 
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(long long nblk, int kblk, const float* __restrict__ X,
                                                           uint8_t* __restrict__ Q, uint8_t* __restrict__ SF,
                                                           int ka) {
   const int lane = threadIdx.x & 31;
-  const WarpRange wr = warp_range((nblk + 3) / 4, kMxUnroll);
+  const WarpRange wr = warp_range((nblk + 7) / 8, kMxUnroll);
   if (wr.p0 >= wr.p1) return;
   const bool packed_sf = (kblk & 3) == 0;
-  long long b = wr.p0 * 4 + (lane >> 3);   // this lane's block
+  long long b = wr.p0 * 8 + (lane >> 2);   // this lane's block
   int r = int(b / kblk), kb = int(b - (long long)r * kblk);
   for (long long p = wr.p0; p < wr.p1; p += kMxUnroll) {
-    float4 x[kMxUnroll];
+    float4 x[kMxUnroll][2];
 #pragma unroll
     for (int u = 0; u < kMxUnroll; ++u) {
-      const long long bu = b + 4 * u;
-      x[u] = bu < nblk ? __ldcs(reinterpret_cast<const float4*>(X + bu * 32 + 4 * (lane & 7)))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      const long long bu = b + 8 * u;
+      const float4* src = reinterpret_cast<const float4*>(X + bu * 32 + 8 * (lane & 3));
+      x[u][0] = bu < nblk ? __ldcs(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[u][1] = bu < nblk ? __ldcs(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kMxUnroll; ++u) {
-      float a = fmaxf(fmaxf(fabsf(x[u].x), fabsf(x[u].y)), fmaxf(fabsf(x[u].z), fabsf(x[u].w)));
+      float a = fmaxf(fmaxf(fmaxf(fabsf(x[u][0].x), fabsf(x[u][0].y)), fmaxf(fabsf(x[u][0].z), fabsf(x[u][0].w))),
+                      fmaxf(fmaxf(fabsf(x[u][1].x), fabsf(x[u][1].y)), fmaxf(fabsf(x[u][1].z), fabsf(x[u][1].w))));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
       a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
       const int e = mx_exponent(a);
       const float inv = __uint_as_float(uint32_t(127 - e) << 23);   // 2^-e, a normal float for e in [-127, 120]
       const uint32_t code = uint32_t(e + 127);
-      // scale bytes of the pass's four blocks, gathered in lane 0
-      const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 8);
-      const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 16);
-      const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 24);
+      // scale bytes of blocks kb..kb+3, gathered in lanes 0 and 16
+      const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
+      const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
+      const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
       if (b < nblk) {
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[u].x, inv), __fmul_rn(x[u].y, inv));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[u].z, inv), __fmul_rn(x[u].w, inv));
-        *reinterpret_cast<uint32_t*>(Q + b * 32 + 4 * (lane & 7)) = lo | (hi << 16);
+        const uint32_t w0 = cvt_e4m3x2(__fmul_rn(x[u][0].x, inv), __fmul_rn(x[u][0].y, inv)) |
+                            (cvt_e4m3x2(__fmul_rn(x[u][0].z, inv), __fmul_rn(x[u][0].w, inv)) << 16);
+        const uint32_t w1 = cvt_e4m3x2(__fmul_rn(x[u][1].x, inv), __fmul_rn(x[u][1].y, inv)) |
+                            (cvt_e4m3x2(__fmul_rn(x[u][1].z, inv), __fmul_rn(x[u][1].w, inv)) << 16);
+        *reinterpret_cast<uint2*>(Q + b * 32 + 8 * (lane & 3)) = make_uint2(w0, w1);
         if (packed_sf) {
-          if (lane == 0)
+          if ((lane & 15) == 0)
             *reinterpret_cast<uint32_t*>(SF + sf_tiled_offset(r, kb, ka)) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-        } else if ((lane & 7) == 0) {
+        } else if ((lane & 3) == 0) {
           SF[sf_tiled_offset(r, kb, ka)] = uint8_t(code);
         }
       }
-      b += 4;
-      kb += 4;
+      b += 8;
+      kb += 8;
       while (kb >= kblk) {
         kb -= kblk;
         ++r;
@@ -305,7 +310,7 @@ tkg_status tkg_quantize_mxfp8(int rows, int k, const float* X, void* Q, void* sf
   const int kblk = k / 32, ka = (kblk + 3) / 4;
   if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 32), stream) != cudaSuccess) return TKG_ERR_CUDA;
   const long long nblk = (long long)rows * kblk;
-  const int grid = grid_for(quant_mxfp8_kernel, ((nblk + 3) / 4 + kMxUnroll - 1) / kMxUnroll * 32, 256);
+  const int grid = grid_for(quant_mxfp8_kernel, ((nblk + 7) / 8 + kMxUnroll - 1) / kMxUnroll * 32, 256);
   quant_mxfp8_kernel<<<grid, 256, 0, stream>>>(
       nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka);
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
