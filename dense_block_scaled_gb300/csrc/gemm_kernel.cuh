@@ -133,9 +133,23 @@ struct GroupTable {
   int rows[kMaxGroups];
   int sfa_block0[kMaxGroups];
 };
+// Grouped GEMM with the group sizes in device memory (written by an earlier
+// kernel, e.g. a router): the kernel builds the table above in shared memory
+// after its dependency wait.  Negative sizes count as 0; rows past the
+// capacity of A and D (GemmParams::m) are neither read into results nor stored.
+struct GroupDev {
+  const int* sizes;                   // device, `count` entries
+  int count;
+  int n_blocks;
+  int ldd;
+  void* d;
+  const float* tb;
+};
 struct NoGroups {
   int unused;
 };
+template <int GROUPED>
+using GroupArg = std::conditional_t<GROUPED == 1, GroupTable, std::conditional_t<GROUPED == 2, GroupDev, NoGroups>>;
 
 // Where one output tile's operands and results live.
 struct TileCoord {
@@ -248,17 +262,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
   }
 }
 
-template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC, bool GROUPED = false>
+// GROUPED: 0 plain GEMM, 1 grouped with a host-built table, 2 grouped with
+// device-resident group sizes (static schedule only).
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC, int GROUPED = 0>
 __global__ void __launch_bounds__(384, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                const __grid_constant__ CUtensorMap tmD, const GemmParams p,
-                const __grid_constant__ std::conditional_t<GROUPED, GroupTable, NoGroups> gt) {
+                const __grid_constant__ CUtensorMap tmD, const GemmParams p, const __grid_constant__ GroupArg<GROUPED> gt) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
+  static_assert(GROUPED != 2 || SCHED == SCHED_STATIC, "device group sizes need the static schedule");
+  // GROUPED == 2: first tile, first row, rows and first SFA block of each
+  // group, then the tile count
+  __shared__ int s_gtab[GROUPED == 2 ? 4 * kMaxGroups + 2 : 1];
 
   // Programmatic dependent launch: the next kernel may be scheduled onto free
   // SMs from here on (its own dependency wait still holds it until this grid
@@ -294,25 +313,41 @@ __global__ void __launch_bounds__(384, 1)
   auto epi_sig_slot = [&](int w) { return ((never_bar + 40u + 15u) & ~15u) + uint32_t(16 * w); };
   auto clc_resp = [&](uint32_t i) { return epi_sig_slot(C::kEpiWarps) + 16u * i; };
 
+  // group table: the host-built parameter, or the shared-memory copy built
+  // from device sizes (filled after the dependency wait, read only after it)
+  auto tab_tile_start = [&](int g) {
+    if constexpr (GROUPED == 2) return s_gtab[g]; else if constexpr (GROUPED == 1) return gt.tile_start[g]; else return 0;
+  };
+  auto tab_row0 = [&](int g) {
+    if constexpr (GROUPED == 2) return s_gtab[kMaxGroups + 1 + g]; else if constexpr (GROUPED == 1) return gt.row0[g]; else return 0;
+  };
+  auto tab_rows = [&](int g) {
+    if constexpr (GROUPED == 2) return s_gtab[2 * kMaxGroups + 1 + g]; else if constexpr (GROUPED == 1) return gt.rows[g]; else return 0;
+  };
+  auto tab_sfa0 = [&](int g) {
+    if constexpr (GROUPED == 2) return s_gtab[3 * kMaxGroups + 1 + g]; else if constexpr (GROUPED == 1) return gt.sfa_block0[g]; else return 0;
+  };
+
   // Tile t -> operand coordinates for this CTA.
   auto coords = [&](int t) {
     TileCoord tc;
-    if constexpr (GROUPED) {
+    if constexpr (GROUPED != 0) {
       // last group whose first tile is <= t (empty groups are skipped)
       int lo = 0, hi = gt.count;
 #pragma unroll 1
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (gt.tile_start[mid] <= t) lo = mid; else hi = mid;
+        if (tab_tile_start(mid) <= t) lo = mid; else hi = mid;
       }
       const int g = lo;
-      const int tiles_m_g = (gt.tile_start[g + 1] - gt.tile_start[g]) / p.tiles_n;
-      tile_coords(t - gt.tile_start[g], tiles_m_g, p.tiles_n, p.raster_group, tc.mb, tc.nb);
+      const int tiles_m_g = (tab_tile_start(g + 1) - tab_tile_start(g)) / p.tiles_n;
+      tile_coords(t - tab_tile_start(g), tiles_m_g, p.tiles_n, p.raster_group, tc.mb, tc.nb);
       const int local_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
-      tc.a_row = gt.row0[g] + local_row;
-      tc.row_limit = gt.row0[g] + gt.rows[g];
+      tc.a_row = tab_row0(g) + local_row;
+      tc.row_limit = tab_row0(g) + tab_rows(g);
+      if (tc.row_limit > p.m) tc.row_limit = p.m;   // never past the capacity of D
       tc.b_row = g * p.n + tc.nb * BN + int(rank) * C::kBBox;
-      tc.sfa_block = gt.sfa_block0[g] + local_row / 128;
+      tc.sfa_block = tab_sfa0(g) + local_row / 128;
       tc.sfb_block0 = g * gt.n_blocks + (tc.nb * BN) / 128;
       tc.group = g;
     } else {
@@ -365,7 +400,7 @@ __global__ void __launch_bounds__(384, 1)
   // previous kernel may still be running (prefetches read nothing back; see
   // ptx::tma_prefetch_2d).
   if (warp == 0) {
-    if (ptx::elect_one() && int(blockIdx.x) / CG < p.num_tiles) {
+    if (GROUPED != 2 && ptx::elect_one() && int(blockIdx.x) / CG < p.num_tiles) {
       const TileCoord tc = coords(int(blockIdx.x) / CG);
       const int npf = min(p.num_kstages, STAGES);
 #pragma unroll 1
@@ -381,6 +416,48 @@ __global__ void __launch_bounds__(384, 1)
   // kernel's tail; global memory is read only after it has completed.
   ptx::pdl_wait();
 
+  int num_tiles = p.num_tiles;
+  if constexpr (GROUPED == 2) {
+    // group table from the device sizes: one warp scans 32 groups at a time
+    if (warp == 3) {
+      int carry_t = 0, carry_r = 0, carry_b = 0;
+#pragma unroll 1
+      for (int g0 = 0; g0 < gt.count; g0 += 32) {
+        const int g = g0 + lane;
+        int mg = g < gt.count ? __ldg(gt.sizes + g) : 0;
+        if (mg < 0) mg = 0;
+        int tl = ((mg + C::kMmaM - 1) / C::kMmaM) * p.tiles_n, rw = mg, bl = (mg + 127) / 128;
+        // inclusive scans over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int a = __shfl_up_sync(0xffffffffu, tl, o), b = __shfl_up_sync(0xffffffffu, rw, o),
+                    c = __shfl_up_sync(0xffffffffu, bl, o);
+          if (lane >= o) {
+            tl += a;
+            rw += b;
+            bl += c;
+          }
+        }
+        const int tiles_g = ((mg + C::kMmaM - 1) / C::kMmaM) * p.tiles_n;
+        if (g < gt.count) {
+          s_gtab[g] = carry_t + tl - tiles_g;
+          s_gtab[kMaxGroups + 1 + g] = carry_r + rw - mg;
+          s_gtab[2 * kMaxGroups + 1 + g] = mg;
+          s_gtab[3 * kMaxGroups + 1 + g] = carry_b + bl - (mg + 127) / 128;
+        }
+        carry_t += __shfl_sync(0xffffffffu, tl, 31);
+        carry_r += __shfl_sync(0xffffffffu, rw, 31);
+        carry_b += __shfl_sync(0xffffffffu, bl, 31);
+      }
+      if (lane == 0) {
+        s_gtab[gt.count] = carry_t;
+        s_gtab[4 * kMaxGroups + 1] = carry_t;
+      }
+    }
+    __syncthreads();
+    num_tiles = s_gtab[4 * kMaxGroups + 1];
+  }
+
   Ctl ctl;
   ctl.abort_flag = &s_abort;
   ctl.abort_smem = ptx::smem_u32(&s_abort);
@@ -391,6 +468,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
+  const int first_tile = cluster_id < num_tiles ? cluster_id : -1;   // static grids may outnumber the tiles
 
   // Next tile for this cluster.  Static: a fixed stride over the tile list.
   // Cluster launch control: the grid holds one cluster per tile; a running
@@ -402,7 +480,7 @@ __global__ void __launch_bounds__(384, 1)
     if constexpr (!C::kClc) {
       (void)cslot;
       (void)cphase;
-      return t + num_clusters < p.num_tiles ? t + num_clusters : -1;
+      return t + num_clusters < num_tiles ? t + num_clusters : -1;
     } else {
       if (!wait_bar<false>(clc_full(cslot), cphase, ctl)) return -2;
       uint32_t x = 0;
@@ -434,7 +512,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-      for (int t = cluster_id; t >= 0 && ok;) {
+      for (int t = first_tile; t >= 0 && ok;) {
         const TileCoord tc = coords(t);
         const int a_row = tc.a_row;
         const int b_row = tc.b_row;
@@ -510,7 +588,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint16_t mask = (CG == 2) ? uint16_t(0x3) : uint16_t(0x1);
       uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-      for (int t = cluster_id; t >= 0 && ok;) {
+      for (int t = first_tile; t >= 0 && ok;) {
         if (!wait_bar<CG == 2>(acce_bar(acc), accph ^ 1u, ctl)) {
           ok = false;
           break;
@@ -630,7 +708,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t acc = 0, accph = 0;
     uint32_t cslot = 0, cphase = 0;
 #pragma unroll 1
-    for (int t = cluster_id; t >= 0;) {
+    for (int t = first_tile; t >= 0;) {
       const TileCoord tc = coords(t);
       float alpha = alpha0;
       if constexpr (GROUPED) {

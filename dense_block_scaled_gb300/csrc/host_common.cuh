@@ -83,7 +83,7 @@ tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
 
 // Launch one instantiation of the persistent GEMM (or, with GROUPED, of the
 // grouped GEMM over pr.groups groups of rows).
-template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED, bool GROUPED = false>
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED, int GROUPED = 0>
 tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
@@ -105,10 +105,24 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   }
 
   // group table: tiles, rows and scale blocks of each group
-  std::conditional_t<GROUPED, GroupTable, NoGroups> gt{};
+  GroupArg<GROUPED> gt{};
   int b_rows = pr.n, sfa_blocks = ceil_div(pr.m, 128), sfb_blocks = ceil_div(pr.n, 128);
   int total_tiles = ceil_div(pr.m, C::kMmaM) * ceil_div(pr.n, BN), max_tiles_m = ceil_div(pr.m, C::kMmaM);
-  if constexpr (GROUPED) {
+  if constexpr (GROUPED == 2) {
+    // sizes live on the device: size the tensor maps and the grid for the
+    // capacity pr.m (the kernel finds the real tile count itself)
+    if (pr.groups < 1 || pr.groups > kMaxGroups || !pr.m_sizes) return TKG_ERR_INVALID_ARG;
+    gt.sizes = pr.m_sizes;
+    gt.count = pr.groups;
+    gt.n_blocks = ceil_div(pr.n, 128);
+    gt.ldd = pr.n;
+    gt.d = pr.D;
+    gt.tb = pr.tb;
+    b_rows = pr.groups * pr.n;
+    sfa_blocks = ceil_div(pr.m, 128) + pr.groups;
+    sfb_blocks = pr.groups * gt.n_blocks;
+    total_tiles = (ceil_div(pr.m, C::kMmaM) + pr.groups) * ceil_div(pr.n, BN);
+  } else if constexpr (GROUPED == 1) {
     if (pr.groups < 1 || pr.groups > kMaxGroups || !pr.m_sizes) return TKG_ERR_INVALID_ARG;
     const int tiles_n = ceil_div(pr.n, BN);
     gt.count = pr.groups;
@@ -342,10 +356,14 @@ inline int choose_split(const Problem& pr, int stage_k) {
 }
 
 // Cluster launch control unless TKG_OPT_SCHEDULER asks for the static schedule.
-template <int FMT, int CG, int BN, int STAGES, int ACC, bool GROUPED = false>
+template <int FMT, int CG, int BN, int STAGES, int ACC, int GROUPED = 0>
 tkg_status launch_sched(const Problem& pr, cudaStream_t s) {
-  if (option(TKG_OPT_SCHEDULER) == 1) return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC, GROUPED>(pr, s);
-  return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_CLC, GROUPED>(pr, s);
+  if constexpr (GROUPED == 2) {
+    return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC, GROUPED>(pr, s);
+  } else {
+    if (option(TKG_OPT_SCHEDULER) == 1) return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_STATIC, GROUPED>(pr, s);
+    return launch_gemm<FMT, CG, BN, STAGES, ACC, SCHED_CLC, GROUPED>(pr, s);
+  }
 }
 
 tkg_status launch_bf16(const Problem& pr, cudaStream_t s);
@@ -354,5 +372,8 @@ tkg_status launch_nvfp4(const Problem& pr, cudaStream_t s);
 tkg_status launch_grouped_bf16(const Problem& pr, cudaStream_t s);
 tkg_status launch_grouped_mxfp8(const Problem& pr, cudaStream_t s);
 tkg_status launch_grouped_nvfp4(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_dev_bf16(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_dev_mxfp8(const Problem& pr, cudaStream_t s);
+tkg_status launch_grouped_dev_nvfp4(const Problem& pr, cudaStream_t s);
 
 }  // namespace tkg

@@ -279,6 +279,62 @@ tkg_status tkg_gemm_grouped_nvfp4(int groups, const int* m_sizes, int n, int k, 
   return launch_grouped_nvfp4(pr, stream);
 }
 
+// Device-resident group sizes: checks shared by the three formats.
+static tkg_status check_grouped_dev(int groups, const int* m_sizes_dev, int m_capacity, int n, int k, const void* A,
+                                    const void* B, void* D, int k_multiple, bool* empty, cudaStream_t stream) {
+  *empty = false;
+  if (groups < 1 || !m_sizes_dev || m_capacity < 0 || n < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (groups > kMaxGroups) return TKG_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(m_sizes_dev) & 3u) return TKG_ERR_ALIGNMENT;
+  if (m_capacity == 0 || n == 0) {
+    *empty = true;
+    return TKG_OK;
+  }
+  if (k == 0) return TKG_ERR_UNSUPPORTED;   // the rows to zero are known only on the device
+  return check_common(m_capacity, n, k, A, B, D, k_multiple, empty, stream);
+}
+
+tkg_status tkg_gemm_grouped_dev_bf16(int groups, const int* m_sizes_dev, int m_capacity, int n, int k, const void* A,
+                                     const void* B, void* D, float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_grouped_dev(groups, m_sizes_dev, m_capacity, n, k, A, B, D, 8, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  Problem pr{m_capacity, n, k, A, B, nullptr, nullptr, nullptr, nullptr, D, alpha, groups, m_sizes_dev};
+  return launch_grouped_dev_bf16(pr, stream);
+}
+
+tkg_status tkg_gemm_grouped_dev_mxfp8(int groups, const int* m_sizes_dev, int m_capacity, int n, int k, const void* A,
+                                      const void* B, const void* sfa, const void* sfb, void* D, float alpha,
+                                      cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_grouped_dev(groups, m_sizes_dev, m_capacity, n, k, A, B, D, 32, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  Problem pr{m_capacity, n, k, A, B, sfa, sfb, nullptr, nullptr, D, alpha, groups, m_sizes_dev};
+  return launch_grouped_dev_mxfp8(pr, stream);
+}
+
+tkg_status tkg_gemm_grouped_dev_nvfp4(int groups, const int* m_sizes_dev, int m_capacity, int n, int k, const void* A,
+                                      const void* B, const void* sfa, const void* sfb, const float* tensor_scale_a,
+                                      const float* tensor_scales_b, void* D, float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_grouped_dev(groups, m_sizes_dev, m_capacity, n, k, A, B, D, 32, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  if ((tensor_scale_a && (reinterpret_cast<uintptr_t>(tensor_scale_a) & 3u)) ||
+      (tensor_scales_b && (reinterpret_cast<uintptr_t>(tensor_scales_b) & 3u)))
+    return TKG_ERR_ALIGNMENT;
+  Problem pr{m_capacity, n, k, A, B, sfa, sfb, tensor_scale_a, tensor_scales_b, D, alpha, groups, m_sizes_dev};
+  return launch_grouped_dev_nvfp4(pr, stream);
+}
+
+size_t tkg_grouped_dev_scale_bytes(int groups, int m_capacity, int k, int block) {
+  if (groups < 1 || m_capacity < 0) return 0;
+  return tkg_scale_bytes(m_capacity, k, block) + size_t(groups) * tkg_scale_bytes(128, k, block);
+}
+
 size_t tkg_grouped_scale_bytes(int groups, const int* m_sizes, int k, int block) {
   if (groups < 1 || !m_sizes) return 0;
   size_t total = 0;

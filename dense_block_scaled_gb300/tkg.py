@@ -29,7 +29,8 @@ EXPORTS = [
     "tkg_scale_bytes", "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
     "tkg_set_option", "tkg_get_option", "tkg_gemm_bf16_noalloc",
     "tkg_gemm_grouped_bf16", "tkg_gemm_grouped_mxfp8", "tkg_gemm_grouped_nvfp4", "tkg_grouped_scale_bytes",
-    "tkg_gemm_bf16_from_host",
+    "tkg_gemm_bf16_from_host", "tkg_gemm_grouped_dev_bf16", "tkg_gemm_grouped_dev_mxfp8",
+    "tkg_gemm_grouped_dev_nvfp4", "tkg_grouped_dev_scale_bytes",
 ]
 
 _lock = threading.Lock()
@@ -61,6 +62,11 @@ def load() -> ctypes.CDLL:
             lib.tkg_grouped_scale_bytes.argtypes = [i, vp, i, i]
             lib.tkg_grouped_scale_bytes.restype = ctypes.c_size_t
             lib.tkg_gemm_bf16_from_host.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_dev_bf16.argtypes = [i, vp, i, i, i, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_dev_mxfp8.argtypes = [i, vp, i, i, i, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_gemm_grouped_dev_nvfp4.argtypes = [i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
+            lib.tkg_grouped_dev_scale_bytes.argtypes = [i, i, i, i]
+            lib.tkg_grouped_dev_scale_bytes.restype = ctypes.c_size_t
             lib.tkg_get_device_status.argtypes = [vp]
             lib.tkg_status_string.argtypes = [st]
             lib.tkg_status_string.restype = ctypes.c_char_p
@@ -209,6 +215,32 @@ def gemm_bf16_from_host(A_host, B_host, D_host, A_dev, B_dev, D_dev, alpha: floa
     _check(load().tkg_gemm_bf16_from_host(m, n, k, _ptr(A_host), _ptr(B_host), _ptr(D_host), _ptr(A_dev),
                                           _ptr(B_dev), _ptr(D_dev), ctypes.c_float(alpha), _stream(stream)),
            "tkg_gemm_bf16_from_host")
+
+
+def gemm_grouped_dev_bf16(sizes_dev, A, B, D, alpha: float = 1.0, stream=None) -> None:
+    """Grouped BF16 GEMM with the group sizes in a device int32 tensor; A, D hold up to A.shape[0] rows."""
+    g = sizes_dev.numel()
+    _check(load().tkg_gemm_grouped_dev_bf16(g, _ptr(sizes_dev), A.shape[0], B.shape[-2], A.shape[-1], _ptr(A),
+                                            _ptr(B), _ptr(D), ctypes.c_float(alpha), _stream(stream)),
+           "tkg_gemm_grouped_dev_bf16")
+
+
+def gemm_grouped_dev_mxfp8(sizes_dev, A, B, sfa, sfb, D, alpha: float = 1.0, stream=None) -> None:
+    g = sizes_dev.numel()
+    _check(load().tkg_gemm_grouped_dev_mxfp8(g, _ptr(sizes_dev), A.shape[0], B.shape[-2], A.shape[-1], _ptr(A),
+                                             _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(D), ctypes.c_float(alpha),
+                                             _stream(stream)), "tkg_gemm_grouped_dev_mxfp8")
+
+
+def gemm_grouped_dev_nvfp4(sizes_dev, A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, tb=None, stream=None) -> None:
+    g = sizes_dev.numel()
+    _check(load().tkg_gemm_grouped_dev_nvfp4(g, _ptr(sizes_dev), A.shape[0], B.shape[-2], 2 * A.shape[-1], _ptr(A),
+                                             _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
+                                             ctypes.c_float(alpha), _stream(stream)), "tkg_gemm_grouped_dev_nvfp4")
+
+
+def grouped_dev_scale_bytes(groups: int, m_capacity: int, k: int, block: int) -> int:
+    return int(load().tkg_grouped_dev_scale_bytes(groups, m_capacity, k, block))
 
 
 def grouped_scale_bytes(m_sizes, k: int, block: int) -> int:

@@ -121,6 +121,37 @@ tkg_status tkg_gemm_grouped_nvfp4(int groups, const int *m_sizes, int n, int k, 
  * tkg_scale_bytes(m_sizes[g], k, block).  0 for invalid arguments. */
 size_t tkg_grouped_scale_bytes(int groups, const int *m_sizes, int k, int block);
 
+/* Grouped GEMM with the group sizes in DEVICE memory (for instance written by
+ * a router kernel earlier on the stream; read after the work already queued
+ * on `stream`, so no host synchronisation is needed).  Same product and
+ * layouts as tkg_gemm_grouped_*, except:
+ *  - m_sizes_dev: device array of `groups` int32 row counts (4-byte aligned);
+ *    a negative count is taken as 0.
+ *  - m_capacity: rows allocated for A and D (and the bound the sizes are
+ *    expected to respect); rows of A past it are never read and rows of D past
+ *    it never written, whatever the sizes say.
+ *  - SFA: per-group tiled buffers back to back as before; the buffer must hold
+ *    tkg_grouped_dev_scale_bytes(groups, m_capacity, k, bs) bytes (the most any
+ *    split of m_capacity rows into `groups` groups needs).
+ *  - k == 0 gives TKG_ERR_UNSUPPORTED (which rows to zero is known only on the
+ *    device).  m_capacity == 0 or n == 0: nothing to do.
+ *  - Runs the static persistent schedule (the tile count is found on the
+ *    device). */
+tkg_status tkg_gemm_grouped_dev_bf16(int groups, const int *m_sizes_dev, int m_capacity, int n, int k,
+                                     const void *A, const void *B, void *D, float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_grouped_dev_mxfp8(int groups, const int *m_sizes_dev, int m_capacity, int n, int k,
+                                      const void *A, const void *B, const void *sfa, const void *sfb, void *D,
+                                      float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_grouped_dev_nvfp4(int groups, const int *m_sizes_dev, int m_capacity, int n, int k,
+                                      const void *A, const void *B, const void *sfa, const void *sfb,
+                                      const float *tensor_scale_a, const float *tensor_scales_b, void *D,
+                                      float alpha, cudaStream_t stream);
+
+/* Bytes an SFA buffer needs for tkg_gemm_grouped_dev_* with up to m_capacity
+ * rows in `groups` groups: tkg_scale_bytes(m_capacity, k, block) plus
+ * groups * tkg_scale_bytes(128, k, block).  0 for invalid arguments. */
+size_t tkg_grouped_dev_scale_bytes(int groups, int m_capacity, int k, int block);
+
 /* BF16 GEMM on operands in HOST memory (the same product as tkg_gemm_bf16;
  * no counterpart on the pages, which time device-resident GEMMs only).
  * A_host (m x k), B_host (n x k): bfloat16, row-major, read; D_host (m x n):

@@ -92,3 +92,20 @@ def test_grouped_scale_bytes():
     sizes = [0, 1, 128, 129]
     assert tkg.grouped_scale_bytes(sizes, 256, 16) == sum(tkg.scale_bytes(m, 256, 16) for m in sizes)
     assert tkg.grouped_scale_bytes([2, -1], 256, 16) == 0
+
+
+def test_grouped_dev_host_checks():
+    import ctypes
+    from dense_block_scaled_gb300 import tkg
+    lib = tkg.load()
+    f = ctypes.c_float(1.0)
+    fake = ctypes.c_void_p(4096)   # never dereferenced: these calls return before any device work
+    assert lib.tkg_gemm_grouped_dev_bf16(0, fake, 8, 8, 8, None, None, None, f, None) == tkg.ERR_INVALID_ARG
+    assert lib.tkg_gemm_grouped_dev_bf16(2, None, 8, 8, 8, None, None, None, f, None) == tkg.ERR_INVALID_ARG
+    assert lib.tkg_gemm_grouped_dev_bf16(129, fake, 8, 8, 8, None, None, None, f, None) == tkg.ERR_UNSUPPORTED
+    assert lib.tkg_gemm_grouped_dev_bf16(2, ctypes.c_void_p(4098), 8, 8, 8, None, None, None, f, None) == \
+        tkg.ERR_ALIGNMENT
+    assert lib.tkg_gemm_grouped_dev_bf16(2, fake, 0, 8, 8, None, None, None, f, None) == tkg.OK
+    assert lib.tkg_gemm_grouped_dev_bf16(2, fake, 8, 8, 0, None, None, None, f, None) == tkg.ERR_UNSUPPORTED
+    assert tkg.grouped_dev_scale_bytes(4, 1000, 256, 16) == \
+        tkg.scale_bytes(1000, 256, 16) + 4 * tkg.scale_bytes(128, 256, 16)

@@ -148,3 +148,74 @@ def test_grouped_all_empty_and_k0(fmt):
     torch.cuda.synchronize()
     out = D.cpu().numpy()
     assert (out[:6] == 0).all() and (out[6:] == GUARD).all()
+
+
+def run_grouped_dev(fmt, sizes_dev, dev, D, alpha=1.0):
+    A, B, sfa, sfb, ta, tb = dev
+    if fmt == "bf16":
+        tkg.gemm_grouped_dev_bf16(sizes_dev, A, B, D, alpha)
+    elif fmt == "mxfp8":
+        tkg.gemm_grouped_dev_mxfp8(sizes_dev, A, B, sfa, sfb, D, alpha)
+    else:
+        tkg.gemm_grouped_dev_nvfp4(sizes_dev, A, B, sfa, sfb, D, alpha, ta=ta, tb=tb)
+
+
+def _with_capacity(fmt, ops, dev, capacity):
+    """Operands padded to `capacity` rows of A (garbage past the groups) and an
+    SFA buffer of the size the device-size entry points require."""
+    A, B, sfa, sfb, ta, tb = dev
+    extra = capacity - A.shape[0]
+    if extra > 0:   # garbage rows past the groups, of A's own dtype
+        if A.dtype == torch.uint8:
+            pad = torch.randint(0, 256, (extra, A.shape[1]), dtype=torch.int32, device="cuda").to(torch.uint8)
+        else:
+            pad = torch.randn(extra, A.shape[1], device="cuda").to(A.dtype)
+        A = torch.cat([A, pad])
+    if fmt != "bf16":
+        need = tkg.grouped_dev_scale_bytes(len(ops.sizes), capacity, ops.k, oracle.BLOCK[fmt])
+        sfa = torch.cat([sfa, torch.zeros(need - sfa.numel(), dtype=torch.uint8, device="cuda")])
+    return A, B, sfa, sfb, ta, tb
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("sizes", [[1, 0, 300, 129, 7], [128, 256, 384], [0, 0, 5]],
+                         ids=lambda s: "-".join(map(str, s)))
+def test_grouped_device_sizes_equal_host_sizes(fmt, sizes):
+    # the same groups with sizes read on the device: identical bits to the
+    # host-table launch, and no row past the groups written
+    n, k = 264, 512
+    ops = GroupedOperands(fmt, sizes, n, k, seed=3300 + sum(sizes))
+    dev = ops.upload()
+    total = sum(sizes)
+    D_host = torch.empty((total, n), dtype=torch.bfloat16, device="cuda")
+    run_grouped(fmt, sizes, dev, D_host)
+    capacity = total + 100
+    dev_c = _with_capacity(fmt, ops, dev, capacity)
+    D = torch.full((capacity, n), GUARD, dtype=torch.int16, device="cuda")
+    sizes_dev = torch.tensor(sizes, dtype=torch.int32, device="cuda")
+    run_grouped_dev(fmt, sizes_dev, dev_c, D.view(torch.bfloat16))
+    assert tkg.device_status() == tkg.OK
+    out = D.cpu()
+    assert torch.equal(out[:total], D_host.cpu().view(torch.int16))
+    assert (out[total:] == GUARD).all()
+
+
+def test_grouped_device_sizes_negative_and_over_capacity():
+    n, k = 136, 256
+    ops = GroupedOperands("bf16", [5, 0, 7], n, k, seed=3400)
+    dev = ops.upload()
+    D_ref = torch.empty((12, n), dtype=torch.bfloat16, device="cuda")
+    run_grouped("bf16", [5, 0, 7], dev, D_ref)
+    # a negative size counts as 0
+    D = torch.full((12, n), GUARD, dtype=torch.int16, device="cuda")
+    run_grouped_dev("bf16", torch.tensor([5, -3, 7], dtype=torch.int32, device="cuda"), dev, D.view(torch.bfloat16))
+    assert tkg.device_status() == tkg.OK
+    assert torch.equal(D.cpu(), D_ref.cpu().view(torch.int16))
+    # sizes past the capacity: rows up to the capacity are right, nothing beyond is touched
+    big = torch.full((12 + 64, n), GUARD, dtype=torch.int16, device="cuda")
+    Dcap = big[:12]
+    run_grouped_dev("bf16", torch.tensor([5, 0, 500], dtype=torch.int32, device="cuda"), dev, Dcap.view(torch.bfloat16))
+    assert tkg.device_status() == tkg.OK
+    out = big.cpu()
+    assert torch.equal(out[:12], D_ref.cpu().view(torch.int16))
+    assert (out[12:] == GUARD).all()
