@@ -22,11 +22,19 @@
 //               fence.proxy.async sits between the stage wait and the MMA: the TMA
 //               data reaches the MMA through the complete_tx release / try_wait
 //               acquire of the same thread (§一 1.2).
-//   warp 2      tensor-memory allocation and release.
+//   warp 2      tensor-memory allocation and release; with cluster launch
+//               control, the tile scheduler (try_cancel of clusters not yet run).
+//   warp 3      with device-resident group sizes, builds the group table.
 //   warps 4-11  epilogue: tcgen05.ld of the accumulator, release of the
 //               accumulator buffer, alpha scale, BF16 round-to-nearest-even, TMA
-//               store.  Accumulators are double buffered when tensor memory has
-//               room (BF16) so the next tile's MMAs overlap this drain (§二 2.2).
+//               store (row-masked stores where a grouped GEMM's group ends).
+//
+// Tensor memory (512 columns): BF16 either double-buffers a 256-column
+// accumulator, so the next tile's MMAs overlap the drain, or runs dual
+// accumulate on 256 x 512 pair tiles (two N=256 MMAs per K step share the A
+// tile, "ThunderKittens 2.0" §二 2.2); MXFP8 / NVFP4 use one 256-column
+// accumulator and a ring of scale regions.  Tiles of odd waves walk K
+// backwards (serpentine order) to reuse the operand slices still in L2.
 //
 // Every wait is bounded: past the limit a role sets the device status word and
 // an abort flag, all roles leave their loops, in-flight copies and MMAs are
