@@ -399,14 +399,16 @@ def e2e_seconds(w, steps, torch, tkg):
     for _ in range(3):   # warm-up steps, as for the device timing
         step()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
         step()
-    e1.record()
-    e1.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+        evs[i + 1].record()
+    evs[-1].synchronize()
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    total_ms = evs[0].elapsed_time(evs[-1])
+    spread = {"median_ms": per_step[len(per_step) // 2], "min_ms": per_step[0], "max_ms": per_step[-1]}
+    return total_ms / 1e3 / steps, h2d, d2h, spread
 
 
 def cpu_baseline(A, B, size, rows):
@@ -584,9 +586,11 @@ def run_ours(args):
             grouped = grouped_timings([f for f in ("bf16", "mxfp8", "nvfp4")], gg, gt, gn, gk,
                                       min(args.steps, 50), min(args.warmup, 20), torch, tkg, synth)
         if not args.no_e2e:
-            te, h2d, d2h = e2e_seconds(head, args.e2e_steps, torch, tkg)
+            te, h2d, d2h, spread = e2e_seconds(head, args.e2e_steps, torch, tkg)
+            # value: all timed steps (mean); the spread shows steps slowed by host-memory
+            # traffic outside this process (the host link is shared)
             e2e = {"value": world * head.flop / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
+                   "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "step_ms": spread}
 
     cpu = None
     if rank == 0 and not args.no_cpu and head.host is not None:
