@@ -26,7 +26,11 @@ struct Problem {
   float alpha;
   int groups = 0;            // grouped GEMM: number of groups, and their sizes (host)
   const int* m_sizes = nullptr;
+  int ldd = 0;               // row stride of D in elements (0: n); plain GEMMs only
 };
+
+// row stride of D in bytes
+inline uint64_t d_row_bytes(const Problem& pr) { return uint64_t(pr.ldd > 0 ? pr.ldd : pr.n) * 2; }
 
 // ---- options and per-device state (tkg_api.cu)
 int option(tkg_option o);
@@ -166,7 +170,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBBox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
-  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
+  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
     return st;
   if constexpr (C::kScaled) {
@@ -280,7 +284,7 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
     return st;
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::BN, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
-  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, uint64_t(pr.n) * 2, 32, 32,
+  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
     return st;
   if constexpr (C::kScaled) {

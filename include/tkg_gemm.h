@@ -157,11 +157,13 @@ size_t tkg_grouped_dev_scale_bytes(int groups, int m_capacity, int k, int block)
  * A_host (m x k), B_host (n x k): bfloat16, row-major, read; D_host (m x n):
  * written.  A_dev, B_dev, D_dev: caller-owned device buffers of the same
  * sizes used as staging (16-byte aligned); their contents afterwards are
- * unspecified except D_dev = D.  The call copies B, then A in bands of rows on
- * one internal stream, runs each band's GEMM on `stream` as its rows arrive,
- * and copies each band of D back on a second internal stream, so the copies
- * overlap the GEMM; host buffers must be page-locked (cudaHostAlloc /
- * cudaHostRegister) for that overlap.  Asynchronous: everything starts after
+ * unspecified except D_dev = D.  The call copies A and B in bands of rows,
+ * alternating, on one internal stream; each band unlocks a rectangle of D (the
+ * new band against the other operand's bands already copied), whose GEMM runs
+ * on `stream` once the band has landed and which goes back on a second
+ * internal stream as soon as that GEMM is done, so the copies overlap the
+ * GEMM; host buffers must be page-locked (cudaHostAlloc / cudaHostRegister)
+ * for that overlap.  Asynchronous: everything starts after
  * the work already queued on `stream`, and work queued on `stream` afterwards
  * starts after D_host is written.  Concurrent calls from several threads are
  * serialised while they enqueue.  Checks and errors as tkg_gemm_bf16. */

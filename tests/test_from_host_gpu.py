@@ -29,9 +29,10 @@ def _run(ops, m, n, k, alpha=1.0):
 
 
 def test_from_host_equals_device_gemm():
-    # four bands of 2048 rows against the whole GEMM on device-resident operands:
-    # the same products, summed in K order that may run either way per tile
-    # (serpentine order), so equal within the tolerance, band edges included
+    # four bands of A and two of B (eight rectangles of D, launched separately)
+    # against the whole GEMM on device-resident operands: the same products,
+    # summed in a K order that may run either way per tile (serpentine order),
+    # so equal within the tolerance, band edges included
     m, n, k = 8192, 4096, 512
     ops = Operands("bf16", m, n, k, seed=41)
     Dh = _run(ops, m, n, k)
@@ -40,13 +41,15 @@ def test_from_host_equals_device_gemm():
     D = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
     tkg.gemm_bf16(A, B, D)
     got, dev = bf16_to_f64(Dh), bf16_to_f64(D)
-    for r0 in (0, 2040, m - 64):
+    for r0 in (0, 2040, 4088, m - 64):
         ref, S = ops.reference(rows=(r0, 64))
         assert_within_tolerance(got[r0:r0 + 64], ref, S, f"from_host rows {r0}..")
         assert_within_tolerance(got[r0:r0 + 64], dev[r0:r0 + 64], S, f"from_host vs device rows {r0}..")
 
 
-@pytest.mark.parametrize("shape", [(5000, 264, 320), (100, 64, 64), (2049, 136, 96)])
+# (5000, 4104, 96): two ragged bands of each operand, so rectangles of D with
+# ragged rows and columns, stored with D's full row stride
+@pytest.mark.parametrize("shape", [(5000, 264, 320), (100, 64, 64), (2049, 136, 96), (5000, 4104, 96)])
 def test_from_host_matches_oracle(shape):
     m, n, k = shape
     ops = Operands("bf16", m, n, k, seed=43 + m, alpha=0.5)
