@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantiser timings")
+    ap.add_argument("--grouped-decode", default="8,16,4096,7168",
+                    help="experts,rows per expert,N,K of the decode-regime grouped GEMM (empty: skip)")
     ap.add_argument("--grouped", default="8,16384,4096,7168",
                     help="grouped GEMM reported beside the headline: groups,total rows,N,K ('' to skip)")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
@@ -350,6 +352,60 @@ def grouped_timings(formats, groups, total, n, k, steps, warmup, torch, tkg, syn
     return out
 
 
+def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth, hbm_gbs):
+    """Grouped GEMM in the decode regime of a mixture-of-experts layer: `rows`
+    rows per expert, bound by reading the experts' n x k weights from HBM.
+    BF16 and MXFP8 (each group's A rows quantised into its own 128-row scale
+    block); reported as time and fraction of the HBM roofline over all bytes."""
+    sizes = [rows] * groups
+    total = rows * groups
+    a, b = synth.gemm_inputs_f32(total, groups * n, k, GROUPED_SEED + 1)
+    dev = torch.device("cuda")
+    out = {"groups": groups, "rows_per_group": rows, "n": n, "k": k}
+    D = torch.empty((total, n), dtype=torch.bfloat16, device=dev)
+
+    def timed(run):
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        e1.synchronize()
+        if tkg.device_status() != tkg.OK:
+            raise RuntimeError("device status after grouped decode timing")
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    A = torch.from_numpy(synth.bf16_codes(a).view("int16")).view(torch.bfloat16).to(dev)
+    B = torch.from_numpy(synth.bf16_codes(b).view("int16")).view(torch.bfloat16).to(dev).view(groups, n, k)
+    t = timed(lambda: tkg.gemm_grouped_bf16(sizes, A, B, D))
+    byts = (groups * n * k + total * k) * 2 + total * n * 2
+    out["bf16"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    del A, B
+    sfb = tkg.scale_bytes(n, k, 32)
+    blk = tkg.scale_bytes(128, k, 32)
+    A8 = torch.empty((total, k), dtype=torch.uint8, device=dev)
+    SA8 = torch.zeros((tkg.grouped_scale_bytes(sizes, k, 32),), dtype=torch.uint8, device=dev)
+    B8 = torch.empty((groups, n, k), dtype=torch.uint8, device=dev)
+    SB8 = torch.empty((groups * sfb,), dtype=torch.uint8, device=dev)
+    X = torch.from_numpy(a).to(dev)
+    for g in range(groups):
+        r0 = g * rows
+        tkg.quantize_mxfp8(X[r0:r0 + rows].contiguous(), A8[r0:r0 + rows],
+                           SA8[g * blk * ((rows + 127) // 128):][:tkg.scale_bytes(rows, k, 32)])
+        tkg.quantize_mxfp8(torch.from_numpy(b[g * n:(g + 1) * n]).to(dev), B8[g], SB8[g * sfb:(g + 1) * sfb])
+    del X
+    t = timed(lambda: tkg.gemm_grouped_mxfp8(sizes, A8, B8, SA8, SB8, D))
+    byts = groups * (n * k + sfb) + total * k + SA8.numel() + total * n * 2
+    out["mxfp8"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    del A8, SA8, B8, SB8, D
+    torch.cuda.empty_cache()
+    return out
+
+
 def graph_seconds(w, steps, torch, tkg):
     """Seconds per launch when the K launches are replayed from one captured CUDA
     graph: the same kernels without the per-call host work."""
@@ -535,7 +591,7 @@ def run_ours(args):
                 "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
                 "measured_peak_tflops": peak_meas, "input_groups": w.groups}
 
-    by_format, sweep, sweep_scaled, skinny, quant, grouped = {}, {}, {}, {}, {}, {}
+    by_format, sweep, sweep_scaled, skinny, quant, grouped, grouped_decode = {}, {}, {}, {}, {}, {}, {}
     e2e = None
     if rank == 0:
         by_format[hf] = fmt_entry(head, t_head)
@@ -585,6 +641,10 @@ def run_ours(args):
             gg, gt, gn, gk = [int(x) for x in args.grouped.split(",")]
             grouped = grouped_timings([f for f in ("bf16", "mxfp8", "nvfp4")], gg, gt, gn, gk,
                                       min(args.steps, 50), min(args.warmup, 20), torch, tkg, synth)
+        if args.grouped_decode:
+            dg, dr, dn, dk = [int(x) for x in args.grouped_decode.split(",")]
+            grouped_decode = grouped_decode_timings(dg, dr, dn, dk, max(args.steps, 100), min(args.warmup, 50), torch,
+                                                    tkg, synth, pk["hbm_gbs"])
         if not args.no_e2e:
             te, h2d, d2h, spread = e2e_seconds(head, args.e2e_steps, torch, tkg)
             # value: all timed steps (mean); the spread shows steps slowed by host-memory
@@ -624,6 +684,7 @@ def run_ours(args):
             "skinny": skinny,
             "quantize": quant,
             "grouped": grouped,
+            "grouped_decode": grouped_decode,
             "kernel_hash": kernel_hash(),
         }
         print(json.dumps(line), flush=True)
