@@ -52,7 +52,8 @@ def parse_args():
     ap.add_argument("--cpu-rows", type=int, default=768, help="rows of the oracle's CPU-baseline sample")
     ap.add_argument("--head-format", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
                     help="format of the first (timed, clock-sampled) workload; profiling runs pick it")
-    ap.add_argument("--skinny", default="16,128,1024", help="M values of the skinny N=K=8192 GEMMs reported")
+    ap.add_argument("--skinny", default="1,16,128,1024",
+                    help="M values of the skinny N=K=8192 GEMMs reported (1: batch-1 decode)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantiser timings")

@@ -63,6 +63,8 @@ struct GemmParams {
   int inject_stall;          // test hook: the MMA role waits on a barrier nothing arrives on
   int raster_group;          // M-blocks per raster band (see tile_coords)
   int wave;                  // tiles per wave (resident clusters); 0: every tile walks K forwards
+  uint32_t tx_bytes;         // bytes landing on the (leader's) full barrier per stage; the A box may be
+                             // shorter than the tile when M is (rows past it feed only unstored rows)
 };
 
 template <int FMT>
@@ -209,8 +211,11 @@ struct GemmConfig {
   static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kFixedBytes;
-  // bytes landing on the leader's full barrier per stage (all CTAs of the pair)
-  static constexpr uint32_t kTxBytes = uint32_t(CG * (kABytes + kBBytes + kSfaBytes + kSfbBytes));
+  // bytes landing on the leader's full barrier per stage (all CTAs of the pair),
+  // for A boxes of a_rows rows
+  static constexpr uint32_t tx_bytes(int a_rows) {
+    return uint32_t(CG * (a_rows * kRowBytes + kBBytes + kSfaBytes + kSfbBytes));
+  }
   // tensor memory: ACC accumulators of BN columns, then a ring of scale
   // regions (4 columns of A scales + 4 per 128-row block of B scales), one
   // region per stage (MXFP8) or per MMA (NVFP4)
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(384, 1)
           armed &= ~(1u << stage);   // its previous load was consumed, hence complete
           const uint32_t fb = lead_full0 + 8u * stage;
           if (leader) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }

@@ -116,6 +116,7 @@ extern "C" tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void* A, 
   p.inject_stall = 0;
   p.raster_group = 8;
   p.wave = 0;
+  p.tx_bytes = C::tx_bytes(C::kCtaM);
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;

@@ -56,7 +56,10 @@ struct SplitKConfig {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kTxBytes = uint32_t(kABytes + kBBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
+  // bytes per stage for A boxes of a_rows rows (at most AROWS)
+  static constexpr uint32_t tx_bytes(int a_rows) {
+    return uint32_t(a_rows * kRowBytes + kBBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
+  }
   static constexpr int kAccCols = BN;
   static constexpr int kScaleBase = BN;
   static constexpr int kRegionCols = 8;                  // 4 columns of A scales, 4 of B scales
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        ptx::mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+        ptx::mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);

@@ -165,7 +165,13 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   const uint64_t row_bytes = FMT == FMT_BF16 ? uint64_t(pr.k) * 2 : kdim;
   const uint32_t boxk = bf16 ? 64 : 128;
   tkg_status st;
-  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, C::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+  // A box: the CTA's 128 rows, or all of M when M is shorter (measured: a box
+  // that runs mostly past the last row slows the load stream, by a third at
+  // M=1).  A grouped tile starts at its group's first row, so its box may still
+  // run past the end, by fewer rows than M.
+  const int a_rows = pr.m < C::kCtaM ? pr.m : C::kCtaM;
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      TKG_OK)
     return st;
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBBox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
@@ -251,6 +257,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   cfg.gridDim = dim3(clusters * CG, 1, 1);
 
   p.wave = max_clusters;   // the serpentine K order flips every wave of resident clusters
+  p.tx_bytes = C::tx_bytes(a_rows);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p, gt);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -280,7 +287,9 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   const uint64_t row_bytes = FMT == FMT_BF16 ? uint64_t(pr.k) * 2 : kdim;
   const uint32_t boxk = bf16 ? 64 : 128;
   tkg_status st;
-  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, AROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+  const int a_rows = pr.m < AROWS ? pr.m : AROWS;   // no A box partly past the last row (see launch_gemm)
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      TKG_OK)
     return st;
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::BN, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
@@ -316,6 +325,7 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
   p.wave = 0;
+  p.tx_bytes = C::tx_bytes(a_rows);
   p.raster_group = raster_group(C::BM, pr.k, FMT, p.tiles_m);
 
   cudaLaunchConfig_t cfg = {};

@@ -96,6 +96,16 @@ def test_chained_launches_read_previous_output():
     assert_within_tolerance(bf16_to_f64(D2), ref2, S2, "second launch reads the first's D")
 
 
+@pytest.mark.parametrize("split", [0, 1])
+@pytest.mark.parametrize("m", [1, 2, 7, 8, 9, 31, 100])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_short_a_box(fmt, m, split):
+    # M below the tile height: the A box is exactly M rows (no box partly past
+    # the last row), on the persistent kernel (split=1) and on split-K where it
+    # is chosen; ragged N and K
+    _check(fmt, m, 520, 640, seed=2600 + m, alpha=0.5, split=split)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_alpha_and_k_tail(fmt):
     # K = 4000: not a multiple of any stage depth; alpha != 1
