@@ -5,7 +5,10 @@
 namespace tkg {
 
 tkg_status launch_bf16(const Problem& pr, cudaStream_t s) {
-  const int cg = option(TKG_OPT_CTA_GROUP);
+  // All of N in one 256-column tile: single-CTA tiles (tall, narrow GEMMs ran
+  // 1.6x faster on them than on CTA pairs, which gain nothing there)
+  const int cg_opt = option(TKG_OPT_CTA_GROUP);
+  const int cg = cg_opt != 0 ? cg_opt : (pr.n <= 256 ? 1 : 2);
   // few output tiles (skinny M): split K across a cluster
   const int split = choose_split(pr, FmtTraits<FMT_BF16>::kStageK);
   if (split >= 2 && pr.m <= 32) {

@@ -63,8 +63,10 @@ struct GemmParams {
   int inject_stall;          // test hook: the MMA role waits on a barrier nothing arrives on
   int raster_group;          // M-blocks per raster band (see tile_coords)
   int wave;                  // tiles per wave (resident clusters); 0: every tile walks K forwards
-  uint32_t tx_bytes;         // bytes landing on the (leader's) full barrier per stage; the A box may be
-                             // shorter than the tile when M is (rows past it feed only unstored rows)
+  uint32_t tx_bytes;         // bytes landing on the (leader's) full barrier per stage; the A and B boxes
+                             // may be shorter than the tile (rows past them feed only unstored results)
+  uint32_t idesc;            // MMA instruction descriptor (N may be narrower than the tile for narrow B)
+  int b_cta_rows;            // B rows each CTA of the pair supplies to one MMA
 };
 
 template <int FMT>
@@ -87,6 +89,11 @@ struct FmtTraits<FMT_NVFP4> {
   static constexpr int kMmaK = 64;
   static constexpr int kSfAtoms = 4;      // 16 blocks of 16 = four atoms, one per MMA
 };
+
+// The same instruction descriptor with N (bits 17-22, N >> 3) replaced.
+__host__ __device__ constexpr uint32_t idesc_with_n(uint32_t idesc, int N) {
+  return (idesc & ~(0x3Fu << 17)) | (uint32_t(N >> 3) << 17);
+}
 
 // Instruction descriptor, kind::f16: D = F32, A = B = BF16, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
@@ -212,9 +219,9 @@ struct GemmConfig {
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kFixedBytes;
   // bytes landing on the leader's full barrier per stage (all CTAs of the pair),
-  // for A boxes of a_rows rows
-  static constexpr uint32_t tx_bytes(int a_rows) {
-    return uint32_t(CG * (a_rows * kRowBytes + kBBytes + kSfaBytes + kSfbBytes));
+  // for A boxes of a_rows rows and b_rows rows of B per CTA (both halves when dual)
+  static constexpr uint32_t tx_bytes(int a_rows, int b_rows) {
+    return uint32_t(CG * (a_rows * kRowBytes + b_rows * kRowBytes + kSfaBytes + kSfbBytes));
   }
   // tensor memory: ACC accumulators of BN columns, then a ring of scale
   // regions (4 columns of A scales + 4 per 128-row block of B scales), one
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(384, 1)
       tc.a_row = tab_row0(g) + local_row;
       tc.row_limit = tab_row0(g) + tab_rows(g);
       if (tc.row_limit > p.m) tc.row_limit = p.m;   // never past the capacity of D
-      tc.b_row = g * p.n + tc.nb * BN + int(rank) * C::kBBox;
+      tc.b_row = g * p.n + tc.nb * BN + int(rank) * p.b_cta_rows;
       tc.sfa_block = tab_sfa0(g) + local_row / 128;
       tc.sfb_block0 = g * gt.n_blocks + (tc.nb * BN) / 128;
       tc.group = g;
@@ -367,7 +374,7 @@ __global__ void __launch_bounds__(384, 1)
       tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, tc.mb, tc.nb);
       tc.a_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
       tc.row_limit = p.m;
-      tc.b_row = tc.nb * BN + int(rank) * C::kBBox;
+      tc.b_row = tc.nb * BN + int(rank) * p.b_cta_rows;
       tc.sfa_block = tc.a_row / 128;
       tc.sfb_block0 = (tc.nb * BN) / 128;
       tc.group = 0;
@@ -625,10 +632,10 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
             const uint32_t accum = (it > 0 || j > 0) ? 1u : 0u;
             if constexpr (FMT == FMT_BF16) {
-              ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, accum);
+              ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, p.idesc, accum);
               if constexpr (C::kDual) {
                 const uint64_t bdesc1 = sdesc_sw128(stage_b(stage) + uint32_t(C::kBBytes / 2));
-                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, C::kIdescBase, accum);
+                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, p.idesc, accum);
               }
             } else {
               // scales -> tensor memory from this thread, right before the MMAs that
@@ -645,10 +652,10 @@ __global__ void __launch_bounds__(384, 1)
               }
               const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
               if constexpr (FMT == FMT_MXFP8) {
-                const uint32_t idesc = C::kIdescBase | (uint32_t(j) << 29) | (uint32_t(j) << 4);
+                const uint32_t idesc = p.idesc | (uint32_t(j) << 29) | (uint32_t(j) << 4);
                 ptx::mma_mxf8<CG>(d_tmem, adesc + koff, bdesc + koff, idesc, reg, reg + 4u, accum);
               } else {
-                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, C::kIdescBase, reg, reg + 4u, accum);
+                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, p.idesc, reg, reg + 4u, accum);
               }
               if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= p.k) {
                 if (++region == uint32_t(C::kRegions)) region = 0;

@@ -116,7 +116,9 @@ extern "C" tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void* A, 
   p.inject_stall = 0;
   p.raster_group = 8;
   p.wave = 0;
-  p.tx_bytes = C::tx_bytes(C::kCtaM);
+  p.tx_bytes = C::tx_bytes(C::kCtaM, C::kBRows);
+  p.idesc = C::kIdescBase;
+  p.b_cta_rows = C::kBBox;
 
   int sms = 0;
   if ((st = device_sm_count(&sms)) != TKG_OK) return st;

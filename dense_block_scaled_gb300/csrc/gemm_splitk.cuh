@@ -56,9 +56,9 @@ struct SplitKConfig {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
-  // bytes per stage for A boxes of a_rows rows (at most AROWS)
-  static constexpr uint32_t tx_bytes(int a_rows) {
-    return uint32_t(a_rows * kRowBytes + kBBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
+  // bytes per stage for A boxes of a_rows rows (at most AROWS) and B boxes of b_rows rows (at most BN)
+  static constexpr uint32_t tx_bytes(int a_rows, int b_rows) {
+    return uint32_t(a_rows * kRowBytes + b_rows * kRowBytes + (kScaled ? kSfaBytes + kSfbBytes : 0));
   }
   static constexpr int kAccCols = BN;
   static constexpr int kScaleBase = BN;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t koff = uint64_t((j * 32) >> 4);
           const uint32_t accum = (ks > ks0 || j > 0) ? 1u : 0u;
           if constexpr (FMT == FMT_BF16) {
-            ptx::mma_f16<1>(tmem, adesc + koff, bdesc + koff, C::kIdesc, accum);
+            ptx::mma_f16<1>(tmem, adesc + koff, bdesc + koff, p.idesc, accum);
           } else {
             const int g = (FMT == FMT_NVFP4) ? j : 0;
             const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(384, 1)
               ptx::tmem_cp_32x128b_x4<1>(reg + 4u, sdesc_sf(stage_sfb(stage) + uint32_t(512 * g)));
             }
             if constexpr (FMT == FMT_MXFP8) {
-              const uint32_t idesc = C::kIdesc | (uint32_t(j) << 29) | (uint32_t(j) << 4);
+              const uint32_t idesc = p.idesc | (uint32_t(j) << 29) | (uint32_t(j) << 4);
               ptx::mma_mxf8<1>(tmem, adesc + koff, bdesc + koff, idesc, reg, reg + 4u, accum);
             } else {
-              ptx::mma_nvf4<1>(tmem, adesc + koff, bdesc + koff, C::kIdesc, reg, reg + 4u, accum);
+              ptx::mma_nvf4<1>(tmem, adesc + koff, bdesc + koff, p.idesc, reg, reg + 4u, accum);
             }
             if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= p.k) {
               if (++region == uint32_t(C::kRegions)) region = 0;

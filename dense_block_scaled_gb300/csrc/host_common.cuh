@@ -173,7 +173,15 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, C::kBBox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+  // Narrow B (N at most half the MMA width; not dual, not grouped): the MMA runs
+  // half as wide, each CTA of a pair supplying half its columns, so the tensor
+  // pipe does not compute columns that do not exist; the B box is clipped to N
+  // rows as the A box is to M.
+  const bool narrow = GROUPED == 0 && !C::kDual && pr.n <= C::kMmaN / 2;
+  const int mma_n = narrow ? C::kMmaN / 2 : C::kMmaN;
+  const int b_cta_rows = C::kDual ? C::kBBox : mma_n / CG;
+  const int b_box = (GROUPED == 0 && pr.n < b_cta_rows) ? pr.n : b_cta_rows;
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, uint32_t(b_box), CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
@@ -257,7 +265,9 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   cfg.gridDim = dim3(clusters * CG, 1, 1);
 
   p.wave = max_clusters;   // the serpentine K order flips every wave of resident clusters
-  p.tx_bytes = C::tx_bytes(a_rows);
+  p.tx_bytes = C::tx_bytes(a_rows, C::kDual ? 2 * b_box : b_box);
+  p.idesc = idesc_with_n(C::kIdescBase, mma_n);
+  p.b_cta_rows = b_cta_rows;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p, gt);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -291,7 +301,11 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, C::BN, CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+  // narrow B: an MMA of N = 64 (the tile's 128 columns would be mostly absent), box clipped to N rows
+  const int mma_n = pr.n <= C::BN / 2 ? C::BN / 2 : C::BN;
+  const int b_box = pr.n < mma_n ? pr.n : mma_n;
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, uint32_t(b_box), CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
@@ -325,7 +339,9 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);
   p.wave = 0;
-  p.tx_bytes = C::tx_bytes(a_rows);
+  p.tx_bytes = C::tx_bytes(a_rows, b_box);
+  p.idesc = idesc_with_n(C::kIdesc, mma_n);
+  p.b_cta_rows = mma_n;
   p.raster_group = raster_group(C::BM, pr.k, FMT, p.tiles_m);
 
   cudaLaunchConfig_t cfg = {};

@@ -106,6 +106,20 @@ def test_short_a_box(fmt, m, split):
     _check(fmt, m, 520, 640, seed=2600 + m, alpha=0.5, split=split)
 
 
+@pytest.mark.parametrize("path", ["auto", "pair", "splitk"])
+@pytest.mark.parametrize("n", [8, 16, 56, 64, 120, 128, 136])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_narrow_b(fmt, n, path):
+    # N at most half the MMA width runs a half-width MMA (N=128 on CTA pairs and
+    # single-CTA tiles, 64 on split-K tiles) with the B box clipped to N rows; 136
+    # stays full width.  "auto" picks single-CTA tiles for N <= 256; "pair" forces
+    # CTA pairs.  M = 1000 (ragged tiles) on the persistent kernel, 40 for split-K.
+    if path == "splitk":
+        _check(fmt, 40, n, 640, seed=2700 + n, alpha=0.5, split=0)
+    else:
+        _check(fmt, 1000, n, 640, seed=2700 + n, alpha=0.5, split=1, cta_group=2 if path == "pair" else 0)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemm_alpha_and_k_tail(fmt):
     # K = 4000: not a multiple of any stage depth; alpha != 1
