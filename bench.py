@@ -464,8 +464,9 @@ def e2e_seconds(w, steps, torch, tkg):
     evs[-1].synchronize()
     per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
     total_ms = evs[0].elapsed_time(evs[-1])
-    spread = {"median_ms": per_step[len(per_step) // 2], "min_ms": per_step[0], "max_ms": per_step[-1]}
-    return total_ms / 1e3 / steps, h2d, d2h, spread
+    median_ms = per_step[len(per_step) // 2]
+    spread = {"median_ms": median_ms, "mean_ms": total_ms / steps, "min_ms": per_step[0], "max_ms": per_step[-1]}
+    return median_ms / 1e3, h2d, d2h, spread
 
 
 def cpu_baseline(A, B, size, rows):
@@ -648,10 +649,12 @@ def run_ours(args):
                                                     tkg, synth, pk["hbm_gbs"])
         if not args.no_e2e:
             te, h2d, d2h, spread = e2e_seconds(head, args.e2e_steps, torch, tkg)
-            # value: all timed steps (mean); the spread shows steps slowed by host-memory
-            # traffic outside this process (the host link is shared)
+            # value: the median step.  The host link and host memory are shared with
+            # other jobs on the machine, and a single step stalled by them (tens of ms)
+            # moves the mean of 20 steps by up to 10x; the mean and the spread are kept
             e2e = {"value": world * head.flop / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "step_ms": spread}
+                   "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "stat": f"median of {args.e2e_steps} steps",
+                   "step_ms": spread}
 
     cpu = None
     if rank == 0 and not args.no_cpu and head.host is not None:
