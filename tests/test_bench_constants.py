@@ -1,0 +1,25 @@
+"""The bench's "of the pages' peak" denominators are the dense per-GPU figures
+the pages print for HGX B200, stored with their citation under tests/golden/."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(ROOT, "tests", "golden", name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, value = line.split()
+                vals[key] = float(value)
+    return vals
+
+
+def test_pages_peaks_match_the_spec_table():
+    sys.path.insert(0, ROOT)
+    import bench
+    g = _golden("hgx_b200_dense_peaks.txt")
+    assert bench.PAGES_PEAK_TFLOPS == {"bf16": g["bf16"] * 1000, "mxfp8": g["fp8"] * 1000,
+                                       "nvfp4": g["nvfp4"] * 1000}
