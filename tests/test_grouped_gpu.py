@@ -119,6 +119,16 @@ def test_grouped_matches_oracle(fmt, sizes, cta_group):
     _check(fmt, sizes, 264, 512, seed=3000 + sum(sizes), cta_group=cta_group, alpha=0.5)
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("n", [8, 16, 72])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_narrow_experts(fmt, n, cta_group):
+    # N far below the tile: each expert's B box runs into the next expert's rows
+    # (and past the end of B for the last one); single-row and ragged groups,
+    # the decode regime's shapes
+    _check(fmt, [1, 1, 0, 17, 1, 130], n, 640, seed=3200 + n, cta_group=cta_group, alpha=0.5)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_grouped_many_groups(fmt):
     # 40 groups of 0..200 rows, N a multiple of the tile, K with a ragged last stage
