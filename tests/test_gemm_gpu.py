@@ -350,7 +350,7 @@ def test_full_size_sampled(fmt, size):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
-@pytest.mark.parametrize("m", [16, 128, 1024])
+@pytest.mark.parametrize("m", [1, 16, 128, 1024])
 def test_skinny_full_size(fmt, m):
     n = k = 8192
     ops = Operands(fmt, m, n, k, seed=1004)
@@ -359,3 +359,16 @@ def test_skinny_full_size(fmt, m):
     rows = min(m, 16)
     ref, S = ops.reference(rows=(m - rows, rows))
     assert_within_tolerance(bf16_to_f64(D[m - rows:]), ref, S, f"{fmt} skinny m={m}")
+
+
+@pytest.mark.parametrize("n", [16, 128])
+def test_tall_narrow_full_size(n):
+    # a router-shaped GEMM at full size (single-CTA tiles, half-width MMA, B box
+    # clipped to N): rows sampled across the M range, all columns
+    m, k = 16384, 4096
+    ops = Operands("bf16", m, n, k, seed=1008)
+    D = run_gemm("bf16", ops.upload(), m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    for r0 in (0, 8000, m - 64):
+        ref, S = ops.reference(rows=(r0, 64))
+        assert_within_tolerance(bf16_to_f64(D[r0:r0 + 64]), ref, S, f"tall narrow n={n} rows {r0}..")
