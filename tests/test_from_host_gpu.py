@@ -87,3 +87,16 @@ def test_from_host_k0_and_ordering():
     for o, Dh in zip((o1, o2), outs):
         ref, S = o.reference(rows=(0, 256))
         assert_within_tolerance(bf16_to_f64(Dh)[:256], ref, S, "ordered calls")
+
+
+def test_from_host_full_size_sampled():
+    # the e2e configuration of the bench: M=N=K=16384 from pinned host buffers
+    # (eight bands of each operand, fifteen rectangles of D); rows sampled in
+    # the first and last bands of A, all columns (every band of B)
+    m = n = k = 16384
+    ops = Operands("bf16", m, n, k, seed=1001)
+    Dh = _run(ops, m, n, k)
+    got = bf16_to_f64(Dh)
+    for r0 in (0, 2040, m - 48):
+        ref, S = ops.reference(rows=(r0, 48))
+        assert_within_tolerance(got[r0:r0 + 48], ref, S, f"from_host 16384^3 rows {r0}..")

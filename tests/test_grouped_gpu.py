@@ -235,3 +235,30 @@ def test_grouped_device_sizes_negative_and_over_capacity():
 def test_grouped_decode_full_size(fmt):
     # the bench's decode-regime grouped GEMM: 8 experts x 16 rows, N=4096, K=7168
     _check(fmt, [16] * 8, 4096, 7168, seed=3300)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
+def test_grouped_prefill_full_size_sampled(fmt):
+    # the bench's prefill grouped GEMM (8 experts, 16384 rows in the seeded
+    # 128-row-multiple sizes, N=4096, K=7168): the first and last 32 rows of
+    # every other group against the oracle on that group's own slices
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    sizes = bench.grouped_sizes(8, 16384)
+    n, k = 4096, 7168
+    ops = GroupedOperands(fmt, sizes, n, k, seed=3400)
+    dev = ops.upload()
+    D = torch.empty((sum(sizes), n), dtype=torch.bfloat16, device="cuda")
+    run_grouped(fmt, sizes, dev, D)
+    assert tkg.device_status() == tkg.OK
+    got = bf16_to_f64(D)
+    row0 = np.concatenate([[0], np.cumsum(sizes)])
+    for g in range(0, len(sizes), 2):
+        for r in (0, sizes[g] - 32):
+            a0 = int(row0[g]) + r
+            sfa = ops.sfa[a0:a0 + 32] if ops.sfa is not None else None
+            sfb = ops.sfb[g] if ops.sfb is not None else None
+            ref, S = oracle.gemm(fmt, ops.A[a0:a0 + 32], ops.B[g], sfa, sfb, ops.alphas[g])
+            assert_within_tolerance(got[a0:a0 + 32], ref, S, f"{fmt} group {g} rows {r}..")
