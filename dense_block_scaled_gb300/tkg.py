@@ -46,6 +46,9 @@ class TkgError(RuntimeError):
 def load() -> ctypes.CDLL:
     """Load libtkg.so (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:   # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
