@@ -1,6 +1,7 @@
 """Concurrent use of the library: GEMMs from two host threads on their own
 streams (tensor-map caches are per thread, options and device state shared),
-and interleaved launches on two streams from one thread."""
+interleaved launches on two streams from one thread, and host-operand GEMMs
+from two threads (the copy streams inside the library are shared)."""
 import threading
 
 import numpy as np
@@ -63,3 +64,43 @@ def test_interleaved_streams_one_thread():
     for tag, D in outs:
         ref, S = (ref_a, S_a) if tag == "a" else (ref_b, S_b)
         assert_within_tolerance(bf16_to_f64(D), ref, S, f"stream {tag}")
+
+
+def test_from_host_two_threads():
+    # each thread: its own pinned host operands, staging buffers and stream;
+    # three calls each, enqueued while the other thread enqueues its own
+    cases = [(4096, 2048, 512, 71), (2560, 4104, 256, 72)]
+    prepared = []
+    for m, n, k, seed in cases:
+        ops = Operands("bf16", m, n, k, seed)
+        Ah = torch.from_numpy(np.ascontiguousarray(ops.A).view(np.int16)).view(torch.bfloat16).pin_memory()
+        Bh = torch.from_numpy(np.ascontiguousarray(ops.B).view(np.int16)).view(torch.bfloat16).pin_memory()
+        dev = [torch.empty((m, k), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((n, k), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((m, n), dtype=torch.bfloat16, device="cuda")]
+        outs = [torch.empty((m, n), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        prepared.append((ops, Ah, Bh, dev, outs))
+    errors = []
+
+    def work(i):
+        try:
+            ops, Ah, Bh, dev, outs = prepared[i]
+            s = torch.cuda.Stream()
+            for Dh in outs:
+                tkg.gemm_bf16_from_host(Ah, Bh, Dh, dev[0], dev[1], dev[2], stream=s)
+            s.synchronize()
+        except Exception as e:   # surfaced in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(prepared))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert tkg.device_status() == tkg.OK
+    for ops, _, _, _, outs in prepared:
+        ref, S = ops.reference(rows=(ops.m - 64, 64))
+        for Dh in outs:
+            assert torch.equal(Dh.view(torch.int16), outs[0].view(torch.int16))
+        assert_within_tolerance(bf16_to_f64(outs[0])[ops.m - 64:], ref, S, f"from_host thread {ops.m}x{ops.n}")

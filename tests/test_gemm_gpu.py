@@ -372,3 +372,16 @@ def test_tall_narrow_full_size(n):
     for r0 in (0, 8000, m - 64):
         ref, S = ops.reference(rows=(r0, 64))
         assert_within_tolerance(bf16_to_f64(D[r0:r0 + 64]), ref, S, f"tall narrow n={n} rows {r0}..")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_long_k_single_tile(fmt):
+    # K = 65536 on one 256 x 256 tile: over a thousand ring stages (BF16) through
+    # one accumulation, the stage phases wrapping hundreds of times
+    m, n, k = 256, 256, 65536
+    tkg.set_option(tkg.OPT_SPLIT_K, 1)
+    ops = Operands(fmt, m, n, k, seed=2900)
+    D = run_gemm(fmt, ops.upload(), m, n, k, 1.0)
+    assert tkg.device_status() == tkg.OK
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D), ref, S, f"{fmt} K={k}")
