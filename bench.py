@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--grouped", default="8,16384,4096,7168",
                     help="grouped GEMM reported beside the headline: groups,total rows,N,K ('' to skip)")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
+    ap.add_argument("--vendor", default="",
+                    help="M=N=K sizes at which the vendor library's GEMMs (cuBLAS / cuBLASLt through torch) are timed "
+                         "beside this library's on the same operands, as context (empty: skip)")
     return ap.parse_args()
 
 
@@ -407,6 +410,65 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     return out
 
 
+class VendorGemm:
+    """The vendor library's GEMM on a Workload's resident operands (torch.mm for BF16, torch._scaled_mm
+    for MXFP8 and NVFP4, which read the same tiled scale layout), launched like Workload.launch.  Context
+    only: the headline and every other number on the line come from this library's kernels."""
+
+    def __init__(self, w, torch):
+        self.w, self.torch = w, torch
+        self.groups, self.flop = w.groups, w.flop
+
+    def launch(self, i, _tkg):
+        torch, w = self.torch, self.w
+        A, B, sa, sb, _, _ = w.sets[i % w.groups]
+        D = w.D[i % w.groups]
+        if w.fmt == "bf16":
+            torch.mm(A, B.t(), out=D)
+        elif w.fmt == "mxfp8":
+            torch._scaled_mm(A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn).t(),
+                             scale_a=sa.view(torch.float8_e8m0fnu), scale_b=sb.view(torch.float8_e8m0fnu),
+                             out_dtype=torch.bfloat16, out=D)
+        else:
+            # per-tensor scales left out: alpha does not change the work
+            torch._scaled_mm(A.view(torch.float4_e2m1fn_x2), B.view(torch.float4_e2m1fn_x2).t(),
+                             scale_a=sa.view(torch.float8_e4m3fn), scale_b=sb.view(torch.float8_e4m3fn),
+                             out_dtype=torch.bfloat16, out=D)
+
+
+def vendor_timings(formats, sizes, steps, warmup, l2, torch, tkg, synth, l2_mode, flush_buf):
+    """Per format and size: this library's GEMM and the vendor library's on the same operands, timed the
+    same way (ours, vendor, ours again), and how many outputs of the two differ by more than BF16 rounding."""
+    out = {}
+    for fmt in formats:
+        for s in sizes:
+            key = f"{fmt} {s}"
+            try:
+                w = Workload(fmt, s, SEEDS[fmt], l2, torch, tkg, synth)
+                v = VendorGemm(w, torch)
+                w.launch(0, tkg)
+                ours = w.D[0].float().clone()
+                v.launch(0, tkg)
+                theirs = w.D[0].float()
+                if fmt == "nvfp4":
+                    theirs = theirs * (w.sets[0][4] * w.sets[0][5])
+                # outside the band one BF16 rounding step wide around ours (relative, plus the same of the
+                # mean magnitude for outputs near zero): different summation orders stay inside it
+                band = 2.0 ** -7 * (ours.abs() + ours.abs().mean())
+                outside = int(((ours - theirs).abs() > band).sum())
+                t0 = time_launches(w, steps, warmup, torch, tkg, None, l2_mode, flush_buf)
+                tv = time_launches(v, steps, warmup, torch, tkg, None, l2_mode, flush_buf)
+                t1 = time_launches(w, steps, min(warmup, 100), torch, tkg, None, l2_mode, flush_buf)
+                out[key] = {"ours_tflops": w.flop / t0 / 1e12, "vendor_tflops": w.flop / tv / 1e12,
+                            "ours_again_tflops": w.flop / t1 / 1e12, "input_groups": w.groups,
+                            "outputs_outside_bf16_band": outside, "outputs": int(ours.numel())}
+                del w, v, ours, theirs
+                torch.cuda.empty_cache()
+            except Exception as e:   # a vendor build without the format: reported, not fatal
+                out[key] = {"error": repr(e)[:300]}
+    return out
+
+
 def graph_seconds(w, steps, torch, tkg):
     """Seconds per launch when the K launches are replayed from one captured CUDA
     graph: the same kernels without the per-call host work."""
@@ -594,6 +656,7 @@ def run_ours(args):
                 "measured_peak_tflops": peak_meas, "input_groups": w.groups}
 
     by_format, sweep, sweep_scaled, skinny, quant, grouped, grouped_decode = {}, {}, {}, {}, {}, {}, {}
+    vendor = {}
     e2e = None
     if rank == 0:
         by_format[hf] = fmt_entry(head, t_head)
@@ -647,6 +710,9 @@ def run_ours(args):
             dg, dr, dn, dk = [int(x) for x in args.grouped_decode.split(",")]
             grouped_decode = grouped_decode_timings(dg, dr, dn, dk, max(args.steps, 100), min(args.warmup, 50), torch,
                                                     tkg, synth, pk["hbm_gbs"])
+        if args.vendor:
+            vendor = vendor_timings(formats, [int(x) for x in args.vendor.split(",") if x], args.steps,
+                                    min(args.warmup, 500), l2, torch, tkg, synth, args.l2, flush_buf)
         if not args.no_e2e:
             te, h2d, d2h, spread = e2e_seconds(head, args.e2e_steps, torch, tkg)
             # value: the median step.  The host link and host memory are shared with
@@ -691,6 +757,8 @@ def run_ours(args):
             "grouped_decode": grouped_decode,
             "kernel_hash": kernel_hash(),
         }
+        if vendor:
+            line["vendor_library"] = vendor
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
