@@ -261,25 +261,32 @@ __device__ __forceinline__ void raise_abort(const Ctl& c) {
 
 // Bounded wait for the phase of parity `parity` of barrier `bar` to complete.
 // Returns false when the kernel is aborting (timeout here or elsewhere).
+// Each try sleeps until the phase completes or kWaitSleepNs pass; the abort
+// flag and the time limit are checked between tries, so an abort raised
+// elsewhere is seen within about kWaitSleepNs.
+constexpr uint32_t kWaitSleepNs = 200000u;
 template <bool kClusterScope>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c) {
-#pragma unroll 1
-  for (int i = 0; i < 32; ++i) {
-    if (kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
-  }
+  if (kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
 #pragma unroll 1
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i) {
-      if (kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
-    }
+    if (kClusterScope ? ptx::mbar_try_wait_cluster_sleep(bar, parity, kWaitSleepNs)
+                      : ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs))
+      return true;
     if (*c.abort_flag) return false;
     if (ptx::globaltimer() - t0 > c.timeout_ns) {
       raise_abort(c);
       return false;
     }
   }
+}
+
+// The same wait made by a whole converged warp; the answer is the same in
+// every lane (an abort seen by one lane ends the wait for all).
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Ctl& c) {
+  return __all_sync(0xffffffffu, wait_bar<kClusterScope>(bar, parity, c));
 }
 
 // GROUPED: 0 plain GEMM, 1 grouped with a host-built table, 2 grouped with
@@ -495,8 +502,34 @@ __global__ void __launch_bounds__(384, 1)
   // cluster takes over a cluster that has not started yet (its tile is that
   // cluster's index).  The pair leader's scheduler lane asks; every role reads
   // the answer from its own CTA's copy and releases it.  Returns -1 when no
-  // tile is left, -2 when the kernel is aborting.
+  // tile is left, -2 when the kernel is aborting.  next_tile is called by a
+  // whole converged warp (every lane waits and reads, lane 0 releases),
+  // next_tile_lane by a role that runs in one elected lane.
   auto next_tile = [&](int t, uint32_t& cslot, uint32_t& cphase) -> int {
+    if constexpr (!C::kClc) {
+      (void)cslot;
+      (void)cphase;
+      return t + num_clusters < num_tiles ? t + num_clusters : -1;
+    } else {
+      if (!wait_bar_warp<false>(clc_full(cslot), cphase, ctl)) return -2;
+      uint32_t x = 0;
+      const bool got = ptx::clc_read(clc_resp(cslot), x);
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          ptx::mbar_arrive(clc_empty(cslot));
+        else
+          ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(clc_empty(cslot), 0));
+      }
+      if (++cslot == 2) {
+        cslot = 0;
+        cphase ^= 1u;
+      }
+      return got ? int(x) / CG : -1;
+    }
+  };
+
+  auto next_tile_lane = [&](int t, uint32_t& cslot, uint32_t& cphase) -> int {
     if constexpr (!C::kClc) {
       (void)cslot;
       (void)cphase;
@@ -583,7 +616,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (!ok) break;
-        t = next_tile(t, cslot, cphase);
+        t = next_tile_lane(t, cslot, cphase);
         if (t == -2) ok = false;
       }
       if (!ok && leader) {
@@ -674,7 +707,7 @@ __global__ void __launch_bounds__(384, 1)
           acc = 0;
           accph ^= 1u;
         }
-        t = next_tile(t, cslot, cphase);
+        t = next_tile_lane(t, cslot, cphase);
         if (t == -2) ok = false;
       }
       // every MMA this thread issued has finished before tensor memory goes away
@@ -734,10 +767,12 @@ __global__ void __launch_bounds__(384, 1)
       if constexpr (GROUPED) {
         if (gt.tb) alpha = alpha * __ldg(gt.tb + tc.group);
       }
-      uint32_t ok = 0;
-      if (lane == 0) ok = wait_bar<false>(accf_bar(acc), accph, ctl) ? 1u : 0u;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      // All 32 lanes wait, converged.  The issuing roles above run in one
+      // elected lane (a producer or MMA warp whose 32 lanes ran the loop, with
+      // one lane issuing, measured 5% and 2x slower on NVFP4), but eight
+      // epilogue warps each waiting in lane 0 with 31 lanes parked cost 2-3%
+      // on NVFP4 and BF16 (branch and convergence units busy the whole tile).
+      if (!wait_bar_warp<false>(accf_bar(acc), accph, ctl)) break;
       ptx::tc_fence_after();
       const int row0 = tc.a_row + q * 32;
       // a 32-row box that crosses the end of a group (grouped GEMM) is stored
@@ -831,9 +866,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      int nt = 0;
-      if (lane == 0) nt = next_tile(t, cslot, cphase);
-      t = __shfl_sync(0xffffffffu, nt, 0);
+      t = __shfl_sync(0xffffffffu, next_tile(t, cslot, cphase), 0);
     }
     // the stores need only have read their shared memory before this CTA goes;
     // their global writes are part of the grid's work the next kernel waits for
