@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(384, 1)
   // idle) has nothing to reduce or store
   const bool live = mb * C::BM + q * 32 < p.m;
   if (epi && live) {
-    if (lane == 0) have = wait_bar<false>(accf_bar, 0u, ctl) ? 1u : 0u;
+    // whole-warp waits, converged (as in the persistent kernel's epilogue)
+    have = wait_bar_warp<false>(accf_bar, 0u, ctl) ? 1u : 0u;
     if constexpr (SPLIT > 1) {
       if (warp == 4 && lane == 0 && have) {
         // every MMA of this CTA has completed, so its stage buffers may take
@@ -306,7 +307,6 @@ __global__ void __launch_bounds__(384, 1)
           if (r != rank) ptx::mbar_arrive_relaxed_cluster(ptx::map_to_rank(go_bar, r));
       }
     }
-    have = __shfl_sync(0xffffffffu, have, 0);
     if (have) {
       ptx::tc_fence_after();
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(h * 64);
@@ -328,9 +328,7 @@ __global__ void __launch_bounds__(384, 1)
   const bool mine = owner == int(rank);
   if constexpr (SPLIT > 1) {
     if (epi && have && !mine) {
-      uint32_t ok = 0;
-      if (lane == 0) ok = wait_bar<false>(go_bar, 0u, ctl) ? 1u : 0u;
-      if (__shfl_sync(0xffffffffu, ok, 0)) {
+      if (wait_bar_warp<false>(go_bar, 0u, ctl)) {
         const int slot = int(rank) < owner ? int(rank) : int(rank) - 1;   // this CTA's place among the senders
         const uint32_t dst = ptx::map_to_rank(base + uint32_t(slot * C::kPartialBytes), uint32_t(owner));
         const uint32_t rbar = ptx::map_to_rank(part_bar, uint32_t(owner));
@@ -344,9 +342,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     if (epi && have && mine) {
-      uint32_t ok = 0;
-      if (lane == 0) ok = wait_bar<false>(part_bar, 0u, ctl) ? 1u : 0u;
-      have = __shfl_sync(0xffffffffu, ok, 0);
+      have = wait_bar_warp<false>(part_bar, 0u, ctl) ? 1u : 0u;
       if (have) {
 #pragma unroll 1
         for (int r = 0; r < SPLIT - 1; ++r) {
