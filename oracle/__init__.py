@@ -73,6 +73,8 @@ def _load():
             lib.orc_quant_mxfp8.restype = i32
             lib.orc_quant_nvfp4.argtypes = [i64, i64, vp, vp, vp, i64]
             lib.orc_quant_nvfp4.restype = ctypes.c_float
+            lib.orc_quant_nvfp4_given.argtypes = [i64, i64, vp, vp, vp, i64, ctypes.c_float]
+            lib.orc_quant_nvfp4_given.restype = i32
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = i32
             _lib = lib
@@ -214,15 +216,21 @@ def quant_mxfp8(X):
     return Q, SF
 
 
-def quant_nvfp4(X):
-    """FP32 (rows, K) -> (packed E2M1 (rows, K/2), E4M3 scales (rows, ld_sf), FP32 tensor scale)."""
+def quant_nvfp4(X, t=None):
+    """FP32 (rows, K) -> (packed E2M1 (rows, K/2), E4M3 scales (rows, ld_sf), FP32 tensor scale).
+
+    With t given, that FP32 tensor scale is used instead of amax / 2688 (values
+    above 6 * 448 * t saturate) and returned as is."""
     X = np.ascontiguousarray(X, dtype=np.float32)
     rows, k = X.shape
     ld = ld_sf(k, "nvfp4")
     Q = np.empty((rows, k // 2), dtype=np.uint8)
     SF = np.zeros((rows, ld), dtype=np.uint8)
-    t = _load().orc_quant_nvfp4(rows, k, _ptr(X), _ptr(Q), _ptr(SF), ld)
-    if t < 0:
+    if t is None:
+        t = _load().orc_quant_nvfp4(rows, k, _ptr(X), _ptr(Q), _ptr(SF), ld)
+        if t < 0:
+            raise ValueError("K must be a multiple of 16")
+    elif _load().orc_quant_nvfp4_given(rows, k, _ptr(X), _ptr(Q), _ptr(SF), ld, float(np.float32(t))) != 0:
         raise ValueError("K must be a multiple of 16")
     return Q, SF, np.float32(t)
 

@@ -314,26 +314,20 @@ int orc_quant_mxfp8(int64_t rows, int64_t K, const float *X, uint8_t *Q,
     return 0;
 }
 
-/* NVFP4:
- *   t   = fp32(amax_tensor / 2688)                     (2688 = 6 * 448)
+/* NVFP4 with the tensor scale t given (the rule below without its first step):
  *   per 1x16 block along K:
  *   d   = fp32(6 * t);  s = RNE_sat_E4M3(fp32(blockamax / d))
  *   den = fp32(dec(s) * t)
  *   q   = RNE_sat_E2M1(fp32(x / den))
- * An all-zero tensor gives t = 0; a block whose scale decodes to 0 gets
- * q = 0 (no division by zero).  Element 2j of a row goes to the low nibble
- * of byte j.  K must be even.  Returns t. */
-float orc_quant_nvfp4(int64_t rows, int64_t K, const float *X, uint8_t *Q,
-                      uint8_t *SF, int64_t ld_sf) {
+ * t <= 0 (or NaN) gives s = 0 and q = 0 everywhere; a block whose scale
+ * decodes to 0 gets q = 0 (no division by zero).  A block whose maximum is
+ * above 6 * 448 * t saturates: s = 448, and codes of quotients above 6 are 6.
+ * Element 2j of a row goes to the low nibble of byte j.  K must be a multiple
+ * of 16.  Returns 0, or -1 for a bad K or ld_sf. */
+int orc_quant_nvfp4_given(int64_t rows, int64_t K, const float *X, uint8_t *Q,
+                          uint8_t *SF, int64_t ld_sf, float t) {
     build_tables();
-    if (K % 16 != 0 || ld_sf < K / 16) return -1.0f;
-    float amax = 0.0f;
-    for (int64_t i = 0; i < rows * K; ++i) {
-        float a = fabsf(X[i]);
-        if (a > amax) amax = a;
-    }
-    volatile float amax_v = amax;
-    float t = amax_v / 2688.0f;
+    if (K % 16 != 0 || ld_sf < K / 16) return -1;
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t b = 0; b < K / 16; ++b) {
@@ -364,5 +358,24 @@ float orc_quant_nvfp4(int64_t rows, int64_t K, const float *X, uint8_t *Q,
             }
         }
     }
+    return 0;
+}
+
+/* NVFP4:
+ *   t   = fp32(amax_tensor / 2688)                     (2688 = 6 * 448)
+ *   then the per-block steps of orc_quant_nvfp4_given with that t.
+ * An all-zero tensor gives t = 0 (all codes 0).  Returns t, or -1 for a bad
+ * K or ld_sf. */
+float orc_quant_nvfp4(int64_t rows, int64_t K, const float *X, uint8_t *Q,
+                      uint8_t *SF, int64_t ld_sf) {
+    if (K % 16 != 0 || ld_sf < K / 16) return -1.0f;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < rows * K; ++i) {
+        float a = fabsf(X[i]);
+        if (a > amax) amax = a;
+    }
+    volatile float amax_v = amax;
+    float t = amax_v / 2688.0f;
+    if (orc_quant_nvfp4_given(rows, K, X, Q, SF, ld_sf, t) != 0) return -1.0f;
     return t;
 }

@@ -200,6 +200,43 @@ def test_quant_nvfp4_rules():
     assert np.all(SF[3, 1] == 0)
 
 
+def test_quant_nvfp4_given_scale_closed_forms():
+    # the NVFP4 rule with the tensor scale supplied, t = 2^-10, every step exact:
+    #   block 0: max 12t -> s = E4M3(12t / 6t) = 2.0 (0x40), den = 2t; 12t -> 6 (0x7),
+    #            3t -> 1.5 (0x3), -t -> -0.5 (0x9)
+    #   block 1: max 10000t is above 6 * 448 * t: s saturates at 448 (0x7E), den = 448t;
+    #            10000t / den = 22.3 saturates to 6 (0x7); 448t -> 1.0 (0x2)
+    #   block 2: all zero -> s = 0, codes 0
+    #   block 3: max 6 * 2^-9 * t -> s = 2^-9, the smallest E4M3 subnormal (0x01); that max -> 6
+    t = np.float32(2.0 ** -10)
+    x = np.zeros((1, 64), np.float32)
+    x[0, 0], x[0, 1], x[0, 2] = 12 * t, 3 * t, -t
+    x[0, 16], x[0, 17] = 10000 * t, 448 * t
+    x[0, 48] = 6 * t * np.float32(2.0 ** -9)
+    Q, SF, tt = oracle.quant_nvfp4(x, t=t)
+    assert tt == t
+    assert list(SF[0, :4]) == [0x40, 0x7E, 0x00, 0x01]
+    want = np.zeros(32, np.uint8)
+    want[0], want[1], want[8], want[24] = 0x37, 0x09, 0x27, 0x07
+    assert np.array_equal(Q[0], want)
+    # decoded, the saturated element sits at the ceiling 6 * 448 * t
+    e2m1, e4m3 = oracle.decode_table("e2m1"), oracle.decode_table("e4m3")
+    assert e2m1[Q[0, 8] & 0xF] * e4m3[SF[0, 1]] * float(t) == 2688 * float(t)
+
+
+def test_quant_nvfp4_given_scale_agrees_with_amax_rule():
+    # given its own amax / 2688, the given-scale path reproduces the full rule;
+    # t <= 0 gives all-zero codes and scales
+    a, _ = synth.gemm_inputs_f32(9, 1, 160, seed=13)
+    Q0, SF0, t0 = oracle.quant_nvfp4(a)
+    assert t0 == np.float32(np.float32(np.abs(a).max()) / np.float32(2688))
+    Q1, SF1, _ = oracle.quant_nvfp4(a, t=t0)
+    assert np.array_equal(Q0, Q1) and np.array_equal(SF0, SF1)
+    for bad in (0.0, -1.0):
+        Q2, SF2, _ = oracle.quant_nvfp4(a, t=bad)
+        assert not Q2.any() and not SF2.any()
+
+
 def test_quant_nvfp4_zero_tensor():
     Q, SF, t = oracle.quant_nvfp4(np.zeros((4, 64), np.float32))
     assert t == 0.0 and not Q.any() and not SF.any()
