@@ -359,8 +359,9 @@ def grouped_timings(formats, groups, total, n, k, steps, warmup, torch, tkg, syn
 def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth, hbm_gbs):
     """Grouped GEMM in the decode regime of a mixture-of-experts layer: `rows`
     rows per expert, bound by reading the experts' n x k weights from HBM.
-    BF16 and MXFP8 (each group's A rows quantised into its own 128-row scale
-    block); reported as time and fraction of the HBM roofline over all bytes."""
+    BF16, MXFP8 and NVFP4 (each group's A rows quantised into its own 128-row
+    scale block; NVFP4 with one tensor scale for all of A); reported as time and
+    fraction of the HBM roofline over all bytes."""
     sizes = [rows] * groups
     total = rows * groups
     a, b = synth.gemm_inputs_f32(total, groups * n, k, GROUPED_SEED + 1)
@@ -405,7 +406,32 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     t = timed(lambda: tkg.gemm_grouped_mxfp8(sizes, A8, B8, SA8, SB8, D))
     byts = groups * (n * k + sfb) + total * k + SA8.numel() + total * n * 2
     out["mxfp8"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
-    del A8, SA8, B8, SB8, D
+    del A8, SA8, B8, SB8
+    # NVFP4: one tensor scale for all of A (the experts' rows quantised together, each group into its own
+    # 128-row scale block with the scale of the whole), one per expert for B
+    sfb4 = tkg.scale_bytes(n, k, 16)
+    blk4 = tkg.scale_bytes(128, k, 16)
+    A4 = torch.empty((total, k // 2), dtype=torch.uint8, device=dev)
+    SA4 = torch.zeros((tkg.grouped_scale_bytes(sizes, k, 16),), dtype=torch.uint8, device=dev)
+    B4 = torch.empty((groups, n, k // 2), dtype=torch.uint8, device=dev)
+    SB4 = torch.empty((groups * sfb4,), dtype=torch.uint8, device=dev)
+    TA = torch.empty(1, dtype=torch.float32, device=dev)
+    TB = torch.empty(groups, dtype=torch.float32, device=dev)
+    X = torch.from_numpy(a).to(dev)
+    whole_q = torch.empty((total, k // 2), dtype=torch.uint8, device=dev)
+    whole_s = torch.empty((tkg.scale_bytes(total, k, 16),), dtype=torch.uint8, device=dev)
+    tkg.quantize_nvfp4(X, whole_q, whole_s, TA)             # the tensor scale of all of A
+    for g in range(groups):
+        r0 = g * rows
+        tkg.quantize_nvfp4_scaled(X[r0:r0 + rows], A4[r0:r0 + rows],
+                                  SA4[g * blk4 * ((rows + 127) // 128):][:tkg.scale_bytes(rows, k, 16)], TA)
+        tkg.quantize_nvfp4(torch.from_numpy(b[g * n:(g + 1) * n]).to(dev), B4[g], SB4[g * sfb4:(g + 1) * sfb4],
+                           TB[g:g + 1])
+    del X, whole_q, whole_s
+    t = timed(lambda: tkg.gemm_grouped_nvfp4(sizes, A4, B4, SA4, SB4, D, ta=TA, tb=TB))
+    byts = groups * (n * k // 2 + sfb4) + total * k // 2 + SA4.numel() + total * n * 2
+    out["nvfp4"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    del A4, SA4, B4, SB4, TA, TB, D
     torch.cuda.empty_cache()
     return out
 

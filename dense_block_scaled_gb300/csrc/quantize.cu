@@ -338,6 +338,23 @@ tkg_status tkg_quantize_nvfp4(int rows, int k, const float* X, void* Q, void* sf
   return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
 }
 
+tkg_status tkg_quantize_nvfp4_scaled(int rows, int k, const float* X, void* Q, void* sf, const float* tensor_scale,
+                                     cudaStream_t stream) {
+  if (rows < 0 || k < 0) return TKG_ERR_INVALID_ARG;
+  if (!tensor_scale) return TKG_ERR_INVALID_ARG;
+  if (!aligned(tensor_scale, 4)) return TKG_ERR_ALIGNMENT;
+  if (rows == 0 || k == 0) return TKG_OK;
+  if (!X || !Q || !sf) return TKG_ERR_INVALID_ARG;
+  if (k % 32 != 0 || !aligned(X, 16) || !aligned(Q, 16) || !aligned(sf, 16)) return TKG_ERR_ALIGNMENT;
+  const int kblk = k / 16, ka = (kblk + 3) / 4;
+  if (cudaMemsetAsync(sf, 0, tkg_scale_bytes(rows, k, 16), stream) != cudaSuccess) return TKG_ERR_CUDA;
+  const long long nblk = (long long)rows * kblk;
+  const int grid = grid_for(quant_nvfp4_kernel, ((nblk + 31) / 32 + kNvUnroll - 1) / kNvUnroll * 32, 256);
+  quant_nvfp4_kernel<<<grid, 256, 0, stream>>>(
+      nblk, kblk, X, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(sf), ka, tensor_scale);
+  return cudaGetLastError() == cudaSuccess ? TKG_OK : TKG_ERR_CUDA;
+}
+
 tkg_status tkg_scales_to_tiled(int rows, int kblocks, const void* src, int ld, void* dst, cudaStream_t stream) {
   if (rows < 0 || kblocks < 0 || ld < kblocks) return TKG_ERR_INVALID_ARG;
   if (rows == 0 || kblocks == 0) return TKG_OK;

@@ -30,7 +30,7 @@ EXPORTS = [
     "tkg_set_option", "tkg_get_option", "tkg_gemm_bf16_noalloc",
     "tkg_gemm_grouped_bf16", "tkg_gemm_grouped_mxfp8", "tkg_gemm_grouped_nvfp4", "tkg_grouped_scale_bytes",
     "tkg_gemm_bf16_from_host", "tkg_gemm_grouped_dev_bf16", "tkg_gemm_grouped_dev_mxfp8",
-    "tkg_gemm_grouped_dev_nvfp4", "tkg_grouped_dev_scale_bytes",
+    "tkg_gemm_grouped_dev_nvfp4", "tkg_grouped_dev_scale_bytes", "tkg_quantize_nvfp4_scaled",
 ]
 
 _lock = threading.Lock()
@@ -78,10 +78,12 @@ def load() -> ctypes.CDLL:
             lib.tkg_scales_to_tiled.argtypes = [i, i, vp, i, vp, vp]
             lib.tkg_quantize_mxfp8.argtypes = [i, i, vp, vp, vp, vp]
             lib.tkg_quantize_nvfp4.argtypes = [i, i, vp, vp, vp, vp, vp]
+            lib.tkg_quantize_nvfp4_scaled.argtypes = [i, i, vp, vp, vp, vp, vp]
             lib.tkg_set_option.argtypes = [i, i]
             lib.tkg_get_option.argtypes = [i]
             for name in ("tkg_gemm_bf16", "tkg_gemm_bf16_noalloc", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status",
-                         "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4", "tkg_set_option",
+                         "tkg_scales_to_tiled", "tkg_quantize_mxfp8", "tkg_quantize_nvfp4",
+                         "tkg_quantize_nvfp4_scaled", "tkg_set_option",
                          "tkg_get_option"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -270,6 +272,13 @@ def quantize_nvfp4(X, Q, sf, tensor_scale, stream=None) -> None:
     rows, k = X.shape
     _check(load().tkg_quantize_nvfp4(rows, k, _ptr(X), _ptr(Q), _ptr(sf), _ptr(tensor_scale), _stream(stream)),
            "tkg_quantize_nvfp4")
+
+
+def quantize_nvfp4_scaled(X, Q, sf, tensor_scale, stream=None) -> None:
+    """NVFP4 codes and tiled scales of X with the given FP32 tensor scale (device, one element, read only)."""
+    rows, k = X.shape
+    _check(load().tkg_quantize_nvfp4_scaled(rows, k, _ptr(X), _ptr(Q), _ptr(sf), _ptr(tensor_scale),
+                                            _stream(stream)), "tkg_quantize_nvfp4_scaled")
 
 
 def device_status(stream=None) -> int:

@@ -231,6 +231,18 @@ tkg_status tkg_quantize_mxfp8(int rows, int k, const float *X, void *Q, void *sf
 tkg_status tkg_quantize_nvfp4(int rows, int k, const float *X, void *Q, void *sf, float *tensor_scale,
                               cudaStream_t stream);
 
+/* The NVFP4 quantiser with the FP32 tensor scale t supplied instead of
+ * computed: the per-block steps above, with t read from tensor_scale (device,
+ * one FP32, not written).  For a calibrated or global activation scale, or to
+ * quantise slices of one tensor (say each expert's rows of a mixture-of-experts
+ * batch, each into its own 128-row scale block) with the scale of the whole.
+ * Blocks whose maximum exceeds 6 * 448 * t saturate (scale 448, codes 6);
+ * t <= 0 or NaN gives all-zero codes and scales.  Q and sf as above.
+ * Errors: tensor_scale NULL -> TKG_ERR_INVALID_ARG, not 4-byte aligned ->
+ * TKG_ERR_ALIGNMENT; otherwise as tkg_quantize_nvfp4. */
+tkg_status tkg_quantize_nvfp4_scaled(int rows, int k, const float *X, void *Q, void *sf, const float *tensor_scale,
+                                     cudaStream_t stream);
+
 /* Process-wide tuning and test options (all default to 0 = automatic). */
 typedef enum {
   TKG_OPT_CTA_GROUP = 1,      /* 0 auto, 1 single-CTA MMA, 2 CTA-pair MMA */

@@ -231,7 +231,7 @@ def test_grouped_device_sizes_negative_and_over_capacity():
     assert (out[12:] == GUARD).all()
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8", "nvfp4"])
 def test_grouped_decode_full_size(fmt):
     # the bench's decode-regime grouped GEMM: 8 experts x 16 rows, N=4096, K=7168
     _check(fmt, [16] * 8, 4096, 7168, seed=3300)

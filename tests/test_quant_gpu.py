@@ -54,6 +54,50 @@ def test_quantize_nvfp4_zero_tensor():
     assert t.item() == 0.0 and not Q.any() and not SF.any()
 
 
+@pytest.mark.parametrize("factor", [1.0, 0.25, 3.0])
+@pytest.mark.parametrize("rows,k", [(130, 96), (1024, 2048), (333, 2080)])
+def test_quantize_nvfp4_scaled_bit_exact(rows, k, factor):
+    # supplied tensor scale: the tensor's own (the codes of tkg_quantize_nvfp4),
+    # a quarter of it (the largest blocks saturate) and three times it
+    x, _ = synth.gemm_inputs_f32(rows, 1, k, seed=3 * rows + k)
+    x[0, 16:32] = 0.0
+    t_own = np.float32(np.float32(np.abs(x).max()) / np.float32(2688))
+    tg = np.float32(t_own * np.float32(factor))
+    Q_ref, SF_ref, _ = oracle.quant_nvfp4(x, t=tg)
+    X = to_dev(x)
+    Q = torch.empty((rows, k // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.full((tkg.scale_bytes(rows, k, 16),), 0xEE, dtype=torch.uint8, device="cuda")
+    T = torch.tensor([float(tg)], dtype=torch.float32, device="cuda")
+    tkg.quantize_nvfp4_scaled(X, Q, SF, T)
+    assert T.item() == float(tg)                      # read, not written
+    assert np.array_equal(Q.cpu().numpy(), Q_ref)
+    assert np.array_equal(SF.cpu().numpy(), tiled_scales(SF_ref, k // 16))
+
+
+def test_quantize_nvfp4_scaled_slices_share_the_scale():
+    # slices of rows quantised with the whole tensor's scale: each slice's codes
+    # are its rows of the whole tensor's codes; a zero scale gives zeros
+    rows, k = 96, 256
+    x, _ = synth.gemm_inputs_f32(rows, 1, k, seed=77)
+    X = to_dev(x)
+    Q = torch.empty((rows, k // 2), dtype=torch.uint8, device="cuda")
+    SF = torch.empty((tkg.scale_bytes(rows, k, 16),), dtype=torch.uint8, device="cuda")
+    T = torch.empty(1, dtype=torch.float32, device="cuda")
+    tkg.quantize_nvfp4(X, Q, SF, T)
+    for r0, r1 in ((0, 16), (16, 48), (48, 96)):
+        Qs = torch.empty((r1 - r0, k // 2), dtype=torch.uint8, device="cuda")
+        SFs = torch.full((tkg.scale_bytes(r1 - r0, k, 16),), 0xEE, dtype=torch.uint8, device="cuda")
+        tkg.quantize_nvfp4_scaled(X[r0:r1], Qs, SFs, T)
+        assert torch.equal(Qs, Q[r0:r1])
+        _, SF_ref, _ = oracle.quant_nvfp4(x[r0:r1], t=np.float32(T.item()))
+        assert np.array_equal(SFs.cpu().numpy(), tiled_scales(SF_ref, k // 16))
+    Z = torch.zeros(1, dtype=torch.float32, device="cuda")
+    Qz = torch.full((rows, k // 2), 0x77, dtype=torch.uint8, device="cuda")
+    SFz = torch.full((tkg.scale_bytes(rows, k, 16),), 0x77, dtype=torch.uint8, device="cuda")
+    tkg.quantize_nvfp4_scaled(X, Qz, SFz, Z)
+    assert not Qz.any() and not SFz.any()
+
+
 @pytest.mark.parametrize("rows,kb", [(1, 1), (130, 7), (300, 125)])
 def test_scales_to_tiled_bit_exact(rows, kb):
     rng = np.random.default_rng(rows)
