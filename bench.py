@@ -570,6 +570,45 @@ def cpu_baseline(A, B, size, rows):
                                         f"(FP64, {dt:.1f} s)"}
 
 
+# The oracle beside the GPU lines: (label, format, m, n, k, seed, rows timed).  Inputs are drawn from the
+# same seeds and quantised by the oracle's own quantisers on the host; a band of rows bounds the larger ones.
+CPU_SWEEP = [
+    ("BF16 M=N=K=512", "bf16", 512, 512, 512, SEEDS["bf16"], 512),
+    ("BF16 M=N=K=2048", "bf16", 2048, 2048, 2048, SEEDS["bf16"], 2048),
+    ("BF16 M=N=K=4096", "bf16", 4096, 4096, 4096, SEEDS["bf16"], 256),
+    ("MXFP8 M=N=K=4096", "mxfp8", 4096, 4096, 4096, SEEDS["mxfp8"], 256),
+    ("NVFP4 M=N=K=4096", "nvfp4", 4096, 4096, 4096, SEEDS["nvfp4"], 256),
+    ("BF16 M=16 N=K=8192", "bf16", 16, 8192, 8192, 1004, 16),
+    ("NVFP4 M=16 N=K=8192", "nvfp4", 16, 8192, 8192, 1004, 16),
+]
+
+
+def cpu_oracle_sweep(configs=CPU_SWEEP):
+    """The oracle, as it stands, timed on each listed configuration (its GEMM only, on `rows` rows of A
+    against all of B), in GFLOP/s."""
+    import oracle
+    from dense_block_scaled_gb300 import synth
+    oracle.build()
+    out = {}
+    for label, fmt, m, n, k, seed, rows in configs:
+        a, b = synth.gemm_inputs_f32(m, n, k, seed)
+        a = a[:rows]
+        if fmt == "bf16":
+            args = (synth.bf16_codes(a), synth.bf16_codes(b))
+        elif fmt == "mxfp8":
+            (qa, sa), (qb, sb) = oracle.quant_mxfp8(a), oracle.quant_mxfp8(b)
+            args = (qa, qb, sa, sb)
+        else:
+            (qa, sa, ta), (qb, sb, tb) = oracle.quant_nvfp4(a), oracle.quant_nvfp4(b)
+            args = (qa, qb, sa, sb, oracle.alpha_eff(1.0, ta, tb))
+        del a, b
+        t0 = time.time()
+        oracle.gemm(fmt, *args)
+        dt = time.time() - t0
+        out[label] = {"gflops": 2.0 * rows * n * k / dt / 1e9, "rows": rows, "seconds": dt}
+    return out
+
+
 # --------------------------------------------------------------------------- arms
 
 def headline_config(size, l2_desc):
@@ -749,8 +788,10 @@ def run_ours(args):
                    "step_ms": spread}
 
     cpu = None
+    cpu_sweep = {}
     if rank == 0 and not args.no_cpu and head.host is not None:
         cpu = cpu_baseline(head.host[0], head.host[1], args.size, args.cpu_rows)
+        cpu_sweep = cpu_oracle_sweep()
 
     if rank == 0:
         name = {"bf16": "BF16", "mxfp8": "MXFP8", "nvfp4": "NVFP4"}[hf]
@@ -785,6 +826,8 @@ def run_ours(args):
         }
         if vendor:
             line["vendor_library"] = vendor
+        if cpu_sweep:
+            line["cpu_oracle_sweep"] = cpu_sweep
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

@@ -23,3 +23,14 @@ def test_pages_peaks_match_the_spec_table():
     g = _golden("hgx_b200_dense_peaks.txt")
     assert bench.PAGES_PEAK_TFLOPS == {"bf16": g["bf16"] * 1000, "mxfp8": g["fp8"] * 1000,
                                        "nvfp4": g["nvfp4"] * 1000}
+
+
+def test_cpu_oracle_sweep_small_configs():
+    # the bench's per-configuration oracle timing, on small shapes of each format
+    sys.path.insert(0, ROOT)
+    import bench
+    out = bench.cpu_oracle_sweep([("bf16", "bf16", 64, 48, 64, 1, 64), ("mxfp8", "mxfp8", 32, 40, 64, 2, 16),
+                                  ("nvfp4", "nvfp4", 32, 40, 64, 3, 8)])
+    assert set(out) == {"bf16", "mxfp8", "nvfp4"}
+    for label, rows in (("bf16", 64), ("mxfp8", 16), ("nvfp4", 8)):
+        assert out[label]["rows"] == rows and out[label]["gflops"] > 0 and out[label]["seconds"] > 0
