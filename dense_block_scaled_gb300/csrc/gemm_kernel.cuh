@@ -597,18 +597,13 @@ __global__ void __launch_bounds__(384, 1)
             const int atom0 = ks * T::kSfAtoms;
             // SFA: this CTA's 128 rows = scale block (a_row / 128)
             ptx::tma_load_3d<CG>(stage_sfa(stage), &tmSFA, 0, atom0, tc.sfa_block, fb, pol_a);
-            // SFB: every CTA of the pair holds the whole N tile's scales.  With a
-            // CTA pair the two 128-row blocks are shared: each CTA fetches one
-            // and multicasts it to both.
-            if constexpr (CG == 2 && C::kSfbBlocks == 2) {
-              ptx::tma_load_3d_mc_pair(stage_sfb(stage) + uint32_t(rank * T::kSfAtoms * 512), &tmSFB, 0, atom0,
-                                       sfb_block0 + int(rank), fb, uint16_t(0x3), pol_b);
-            } else {
+            // SFB: every CTA of the pair holds the whole N tile's scales (the
+            // MMA reads B scales from each CTA's tensor memory), so each CTA
+            // loads every 128-row block itself; plain loads, no multicast.
 #pragma unroll
-              for (int a = 0; a < C::kSfbBlocks; ++a)
-                ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(a * T::kSfAtoms * 512), &tmSFB, 0, atom0,
-                                     sfb_block0 + a, fb, pol_b);
-            }
+            for (int a = 0; a < C::kSfbBlocks; ++a)
+              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(a * T::kSfAtoms * 512), &tmSFB, 0, atom0,
+                                   sfb_block0 + a, fb, pol_b);
           }
           if (++stage == STAGES) {
             stage = 0;

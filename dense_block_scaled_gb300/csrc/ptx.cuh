@@ -229,19 +229,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
   }
 }
 
-// 3-D tiled load multicast to the CTAs of `cta_mask` (same shared-memory offset
-// in each).  With the CTA-pair form the completion of every destination's
-// bytes is counted on the barrier of that destination's pair leader, given by
-// `bar` (the leader's barrier, peer bit clear).
-__device__ __forceinline__ void tma_load_3d_mc_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
-                                                    uint32_t bar, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // Shared memory of this CTA -> shared memory of a CTA in the cluster (async
 // proxy), completion counted on `bar` in the destination CTA.
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
