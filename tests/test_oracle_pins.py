@@ -503,3 +503,50 @@ def test_gemm_grouped_bruteforce_fraction(fmt):
                 else:
                     assert Fraction(ref[row + i, j]) == eref[i][j], (g, i, j)
         row += mg
+
+
+# --------------------------------------------------------------------------- NVFP4 per-tensor scales
+
+def _round_f32(x: Fraction) -> Fraction:
+    """x > 0 rounded to the nearest FP32 value, ties to even (normal range),
+    written from the definition: 24 significant bits at x's binade."""
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    q = x / ulp
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return n * ulp
+
+
+def test_alpha_eff_double_rounding_in_fp32():
+    # The NVFP4 per-tensor scales join alpha as fp32(fp32(alpha * tA) * tB): two
+    # FP32 products in that order ("ThunderKittens 2.0 GPU Kernel优化", table of
+    # updates: NVFP4 with its FP32 per-tensor scale).  These operands are exact
+    # FP32 values chosen so that every plausible slip -- one rounding of the
+    # exact product, the other multiplication order, an FP64 product -- gives a
+    # different FP32 result.
+    alpha = 1 + Fraction(1025, 2 ** 23)
+    ta = (1 + Fraction(1, 4096)) * Fraction(1, 2 ** 9)
+    tb = (1 + Fraction(3, 4096)) * Fraction(1, 2 ** 10)
+    for v in (alpha, ta, tb):
+        assert _round_f32(v) == v
+    want = _round_f32(_round_f32(alpha * ta) * tb)
+    slips = {
+        "single rounding": _round_f32(alpha * ta * tb),
+        "tA*tB first": _round_f32(alpha * _round_f32(ta * tb)),
+        "alpha*tB first": _round_f32(_round_f32(alpha * tb) * ta),
+        "fp64 product": Fraction(float(np.float32(float(alpha) * float(ta) * float(tb)))),
+    }
+    for name, v in slips.items():
+        assert v != want, name
+    got = oracle.alpha_eff(float(alpha), float(ta), float(tb))
+    assert Fraction(got) == want
+    # a scale of 1.0 leaves alpha as is, and the default arguments are 1.0
+    assert oracle.alpha_eff(float(alpha)) == float(alpha)
+    assert oracle.alpha_eff(0.75, 1.0, 1.0) == 0.75
