@@ -32,11 +32,11 @@ constexpr size_t kScratchNeeded = sizeof(unsigned int);
 static __device__ __align__(256) unsigned int g_noalloc_scratch[kScratchWords];
 
 std::mutex g_mu;
-unsigned int* g_scratch_dev[64] = {};   // device address of the array, per device
-bool g_attr_set[64] = {};
+unsigned int* g_scratch_dev[64] = {};   // device address of the array, per device (null: not set up)
 
-// One-time set-up for the current device.  Returns the array's device address.
-tkg_status scratch_for_current_device(unsigned int** out, int* dev_out) {
+// One-time set-up for the current device: looks up the array's device address
+// and clears the array (on `stream`).  Returns the address.
+tkg_status scratch_for_current_device(unsigned int** out, cudaStream_t stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TKG_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -46,10 +46,10 @@ tkg_status scratch_for_current_device(unsigned int** out, int* dev_out) {
       cudaGetLastError();
       return TKG_ERR_CUDA;
     }
+    if (cudaMemsetAsync(p, 0, kScratchBytes, stream) != cudaSuccess) return TKG_ERR_CUDA;
     g_scratch_dev[dev] = static_cast<unsigned int*>(p);
   }
   *out = g_scratch_dev[dev];
-  *dev_out = dev;
   return TKG_OK;
 }
 
@@ -73,80 +73,46 @@ extern "C" tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void* A, 
   if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || (k % 8) != 0)
     return TKG_ERR_ALIGNMENT;
 
-  using C = GemmConfig<FMT_BF16, 2, 256, 6, 2>;
-  auto kern = gemm_kernel<FMT_BF16, 2, 256, 6, 2>;
   unsigned int* scratch = nullptr;
-  int dev = 0;
-  tkg_status st = scratch_for_current_device(&scratch, &dev);
+  tkg_status st = scratch_for_current_device(&scratch, stream);
   if (st != TKG_OK) return st;
+  // The status word is an error flag the kernel only ever sets: like the
+  // library's own word it keeps a timeout until tkg_get_device_status reads and
+  // clears it, so no call clears it on entry (which would hide an earlier
+  // call's timeout).  Nothing else in the array is used.
+  // The CTA-pair kernel of tkg_gemm_bf16 on the static persistent schedule,
+  // launched by the same code (A and B boxes clipped to m and n, half-width
+  // MMAs for narrow n), with the status word in the array.
+  Problem pr{m, n, k, A, B, nullptr, nullptr, nullptr, nullptr, D, alpha};
+  pr.status = scratch + kStatusWord;
+  return launch_gemm<FMT_BF16, 2, 256, 6, 2, SCHED_STATIC>(pr, stream);
+}
+
+namespace tkg {
+
+// Status read for tkg_get_device_status: reads the array's status word on the
+// current device and clears it when set (allocates nothing; 0 when this entry
+// point was never set up on the device).
+tkg_status noalloc_take_status(cudaStream_t stream, unsigned int* out) {
+  *out = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TKG_ERR_CUDA;
+  unsigned int* w = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_attr_set[dev]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-        return TKG_ERR_CUDA;
-      g_attr_set[dev] = true;
-    }
+    w = g_scratch_dev[dev];
   }
-
-  CUtensorMap tmA, tmB, tmD;
-  if ((st = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, k, m, uint64_t(k) * 2, 64, C::kCtaM,
-                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
-    return st;
-  if ((st = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, k, n, uint64_t(k) * 2, 64, C::kBRows,
-                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
-    return st;
-  if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, n, m, uint64_t(n) * 2, 32, 32,
-                      CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
-    return st;
-
-  GemmParams p;
-  p.m = m;
-  p.n = n;
-  p.k = k;
-  p.num_kstages = ceil_div(k, FmtTraits<FMT_BF16>::kStageK);
-  p.tiles_m = ceil_div(m, C::kMmaM);
-  p.tiles_n = ceil_div(n, 256);
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  p.alpha = alpha;
-  p.ta = nullptr;
-  p.tb = nullptr;
-  p.status = scratch + kStatusWord;
-  const int tmo = option(TKG_OPT_TIMEOUT_MS);
-  p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
-  p.inject_stall = 0;
-  p.raster_group = 8;
-  p.wave = 0;
-  p.tx_bytes = C::tx_bytes(C::kCtaM, C::kBRows);
-  p.idesc = C::kIdescBase;
-  p.b_cta_rows = C::kBBox;
-
-  int sms = 0;
-  if ((st = device_sm_count(&sms)) != TKG_OK) return st;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
-    cudaGetLastError();
-    clusters = sms / 2;
-  }
-  if (clusters > p.num_tiles) clusters = p.num_tiles;
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-
-  // The array keeps the previous call's contents: the status word must start at zero.
-  if (cudaMemsetAsync(p.status, 0, kScratchNeeded, stream) != cudaSuccess) return TKG_ERR_CUDA;
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmD, tmD, tmD, p, NoGroups{0}) != cudaSuccess) {
-    cudaGetLastError();
+  if (!w) return TKG_OK;
+  unsigned int h = 0;
+  if (cudaMemcpyAsync(&h, w + kStatusWord, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return TKG_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+  if (h != 0) {
+    if (cudaMemsetAsync(w + kStatusWord, 0, sizeof h, stream) != cudaSuccess) return TKG_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
   }
+  *out = h;
   return TKG_OK;
 }
+
+}  // namespace tkg

@@ -27,6 +27,7 @@ struct Problem {
   int groups = 0;            // grouped GEMM: number of groups, and their sizes (host)
   const int* m_sizes = nullptr;
   int ldd = 0;               // row stride of D in elements (0: n); plain GEMMs only
+  unsigned int* status = nullptr;   // device status word to use (null: the library's, allocated on first use)
 };
 
 // row stride of D in bytes
@@ -35,6 +36,10 @@ inline uint64_t d_row_bytes(const Problem& pr) { return uint64_t(pr.ldd > 0 ? pr
 // ---- options and per-device state (tkg_api.cu)
 int option(tkg_option o);
 tkg_status device_status_word(unsigned int** out);   // lazily allocated per device
+unsigned int* existing_status_word();                // the current device's word if allocated, else null
+// allocation-free entry point (gemm_noalloc.cu): reads and clears its status
+// word on the current device (0 when it was never set up there)
+tkg_status noalloc_take_status(cudaStream_t stream, unsigned int* out);
 tkg_status device_sm_count(int* out);
 tkg_status device_l2_bytes(int* out);
 
@@ -212,7 +217,10 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   p.alpha = pr.alpha;
   p.ta = pr.ta;
   p.tb = GROUPED ? nullptr : pr.tb;
-  if ((st = device_status_word(&p.status)) != TKG_OK) return st;
+  if (pr.status)
+    p.status = pr.status;
+  else if ((st = device_status_word(&p.status)) != TKG_OK)
+    return st;
   const int tmo = option(TKG_OPT_TIMEOUT_MS);
   p.timeout_ns = 1000000ull * (unsigned long long)(tmo > 0 ? tmo : 1000);
   p.inject_stall = option(TKG_OPT_INJECT_STALL);

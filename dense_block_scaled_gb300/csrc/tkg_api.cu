@@ -45,6 +45,13 @@ tkg_status device_status_word(unsigned int** out) {
   return TKG_OK;
 }
 
+unsigned int* existing_status_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  return g_status[dev];
+}
+
 tkg_status device_sm_count(int* out) {
   const int dev = current_device();
   if (dev < 0) return TKG_ERR_CUDA;
@@ -347,15 +354,22 @@ size_t tkg_grouped_scale_bytes(int groups, const int* m_sizes, int k, int block)
 
 tkg_status tkg_get_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
-  unsigned int* w = nullptr;
-  tkg_status st = device_status_word(&w);
-  if (st != TKG_OK) return st;
   unsigned int h = 0;
-  if (cudaMemcpyAsync(&h, w, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return TKG_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+  // the library's word exists once an allocating entry point has run on this
+  // device; before that no kernel can have set it, and nothing is allocated here
+  if (unsigned int* w = existing_status_word()) {
+    if (cudaMemcpyAsync(&h, w, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return TKG_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+    if (h != 0) {
+      if (cudaMemsetAsync(w, 0, sizeof h, stream) != cudaSuccess) return TKG_ERR_CUDA;
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
+    }
+  }
+  // the allocation-free entry point's word, in its fixed array
+  unsigned int h2 = 0;
+  if (noalloc_take_status(stream, &h2) != TKG_OK) return TKG_ERR_CUDA;
+  h |= h2;
   if (h == 0) return TKG_OK;
-  if (cudaMemsetAsync(w, 0, sizeof h, stream) != cudaSuccess) return TKG_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return TKG_ERR_CUDA;
   return (h & DEV_ERR_TIMEOUT) ? TKG_ERR_TIMEOUT : TKG_ERR_CUDA;
 }
 

@@ -177,27 +177,33 @@ tkg_status tkg_gemm_bf16_from_host(int m, int n, int k, const void *A_host, cons
  * on the pages: this is a property of the library, not of the method.)
  *
  * Same arguments, layouts, checks and result as tkg_gemm_bf16, and the same
- * kernel.  Its scratch -- the status word the kernel sets when a bounded wait
- * runs out -- lives in a fixed 256-byte array that is part of the library
- * image (each GPU that loads the library keeps it until the process exits)
- * instead of memory obtained with cudaMalloc.  The kernel needs 4 bytes of it
- * whatever m, n and k are; a call whose scratch need exceeded the array would
- * return TKG_ERR_UNSUPPORTED.
+ * CTA-pair kernel on its static persistent schedule.  Its scratch -- the
+ * status word the kernel sets when a bounded wait runs out -- lives in a fixed
+ * 256-byte array that is part of the library image (each GPU that loads the
+ * library keeps it until the process exits) instead of memory obtained with
+ * cudaMalloc.  The kernel needs 4 bytes of it whatever m, n and k are; a call
+ * whose scratch need exceeded the array would return TKG_ERR_UNSUPPORTED.
  *  - The first call on a device does one-time set-up there (it looks up the
- *    array's device address and sets the kernel's shared-memory limit); make
- *    that first call before any stream capture.
- *  - Every call on a device shares the one array and clears the status word
- *    when it starts, so calls that overlap on the GPU race on it: order them
- *    on one stream or with events.
- *  - A timed-out wait in this variant is recorded only in that array, not in
- *    the word tkg_get_device_status reads; D is then unspecified. */
+ *    array's device address, clears the array on `stream` and sets the
+ *    kernel's shared-memory limit); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array, so calls that overlap on the
+ *    GPU race on it: order them on one stream or with events.
+ *  - A timed-out wait sets the array's status word, which no call clears on
+ *    entry; tkg_get_device_status reads it and clears it (allocating nothing),
+ *    as it does the library's own word.  D is then unspecified.
+ *  - Options set with tkg_set_option apply as to tkg_gemm_bf16, except that the
+ *    schedule is always the static one. */
 tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void *A, const void *B, void *D, float alpha,
                                  cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's status
- * word: TKG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
- * call (its output is then unspecified), TKG_ERR_CUDA on a CUDA error,
- * TKG_OK otherwise. */
+ * words: the library's own (created by the first allocating entry point on the
+ * device) and that of tkg_gemm_bf16_noalloc (once set up on the device).
+ * Returns TKG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call (its output is then unspecified), TKG_ERR_CUDA on a CUDA error, TKG_OK
+ * otherwise.  Allocates nothing: a word that does not exist yet reads as
+ * clear. */
 tkg_status tkg_get_device_status(cudaStream_t stream);
 
 /* Static string naming a status code. */
