@@ -48,6 +48,11 @@ def parse_args():
     ap.add_argument("--formats", default="bf16,mxfp8,nvfp4")
     ap.add_argument("--sweep", default="512,2048,4096,8192", help="extra BF16 sizes reported beside the headline")
     ap.add_argument("--sweep-scaled", default="4096,8192", help="extra MXFP8 / NVFP4 sizes reported beside 16384")
+    ap.add_argument("--nontile", default="4000", help="M=N=K sizes that are not tile multiples, timed in BF16 and NVFP4")
+    ap.add_argument("--sustained-s", type=float, default=1.0,
+                    help="seconds of back-to-back headline launches timed after the headline loop (0: skip)")
+    ap.add_argument("--no-vendor-peak", action="store_true",
+                    help="skip timing the vendor library's MXFP8 / NVFP4 GEMM on the 16384 operands (measured peaks)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=768, help="rows of the oracle's CPU-baseline sample")
     ap.add_argument("--head-format", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
@@ -248,6 +253,27 @@ def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flu
     if st != tkg.OK:
         raise RuntimeError(f"device status after timing: {tkg.status_string(st)}")
     return ms / 1e3 / steps
+
+
+def sustained_seconds(w, seconds, t_burst, torch, tkg, uuid):
+    """Seconds per launch over a back-to-back run of at least `seconds` (the
+    part settles at its power cap), with the clocks sampled during it."""
+    n = max(10, int(seconds / max(t_burst, 1e-6)) + 1)
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        w.launch(i, tkg)
+    e1.record()
+    e1.synchronize()
+    clk = clocks.stop()
+    st = tkg.device_status()
+    if st != tkg.OK:
+        raise RuntimeError(f"device status after the sustained loop: {tkg.status_string(st)}")
+    ms = e0.elapsed_time(e1)
+    return ms / 1e3 / n, n, ms / 1e3, clk
 
 
 def quant_timings(X, steps, warmup, torch, tkg, hbm_gbs):
@@ -623,6 +649,27 @@ def l2_description(groups, mode):
     return "inputs larger than 3x L2, no rotation needed" if groups == 1 else f"{groups} rotated input groups"
 
 
+def config_table(by_format, nontile, skinny, size):
+    """The workload definition's configurations in one compact table (TFLOP/s or
+    microseconds and the roofline fractions), for the headline line's roofline
+    object."""
+    name = {"bf16": "BF16", "mxfp8": "MXFP8", "nvfp4": "NVFP4"}
+    keys = ("tflops", "frac_of_pages_peak", "frac_of_measured", "frac_of_nominal")
+    out = {}
+    for fmt, e in by_format.items():
+        out[f"{name[fmt]} {size}^3"] = {k: e.get(k) for k in keys}
+        if e.get("measured_peak_source"):
+            out[f"{name[fmt]} {size}^3"]["measured_peak"] = e["measured_peak_tflops"]
+    for key, e in nontile.items():
+        fmt, s_ = key.split()
+        out[f"{name[fmt]} {s_}^3"] = {k: e.get(k) for k in keys}
+    for key, e in skinny.items():
+        out[key.replace("bf16", "BF16").replace("nvfp4", "NVFP4")] = {
+            "us": e["us"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
+            "frac_of_roofline": e["frac_of_roofline"]}
+    return out
+
+
 def max_over_ranks(t, dist, torch, device):
     """The job's time: the slowest rank's (each rank times the same number of
     steps of its own replica)."""
@@ -712,15 +759,34 @@ def run_ours(args):
     t_max = max_over_ranks(t_head, dist, torch, "cuda")
     value = job_value(world, head.flop, t_max) / 1e12
     achieved = head.flop / t_head / 1e12
+    sustained = None
+    if rank == 0 and args.sustained_s > 0:
+        ts, ns, secs, sclk = sustained_seconds(head, args.sustained_s, t_head, torch, tkg, uuid)
+        tf = head.flop / ts / 1e12
+        sustained = {"tflops": tf, "launches": ns, "seconds": secs, "clocks": sclk,
+                     "frac_of_sustained_peak": (tf / (pk["bf16_sustained"] * NOMINAL_RATIO[hf])
+                                                if pk["bf16_sustained"] else None),
+                     "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[hf]}
+
+    vendor_peak = {}   # the vendor library's same-loop TFLOP/s on the same operands: a measured per-format peak
 
     def fmt_entry(w, t):
         tf = w.flop / t / 1e12
-        peak_meas = pk["bf16"] * NOMINAL_RATIO[w.fmt]
+        nominal = pk["bf16"] * NOMINAL_RATIO[w.fmt]
+        if w.fmt == "bf16":
+            peak_meas, src = pk["bf16"], f"{pk['source']} cuBLAS bf16 burst"
+        elif w.fmt in vendor_peak:
+            peak_meas, src = vendor_peak[w.fmt], "vendor library, same operands, same loop"
+        else:
+            peak_meas, src = None, None
         return {"tflops": tf, "ms": t * 1e3, "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[w.fmt],
-                "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt], "frac_of_measured": tf / peak_meas,
-                "measured_peak_tflops": peak_meas, "input_groups": w.groups}
+                "pages_peak_tflops": PAGES_PEAK_TFLOPS[w.fmt],
+                "measured_peak_tflops": peak_meas, "frac_of_measured": tf / peak_meas if peak_meas else None,
+                "measured_peak_source": src, "nominal_peak_tflops": nominal, "frac_of_nominal": tf / nominal,
+                "input_groups": w.groups}
 
     by_format, sweep, sweep_scaled, skinny, quant, grouped, grouped_decode = {}, {}, {}, {}, {}, {}, {}
+    nontile = {}
     vendor = {}
     e2e = None
     if rank == 0:
@@ -730,8 +796,15 @@ def run_ours(args):
                 continue
             w = Workload(fmt, args.size, SEEDS[fmt], l2, torch, tkg, synth,
                          keep_fp32=(fmt != "bf16" and not args.no_quant and not quant))
-            by_format[fmt] = fmt_entry(w, time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2,
-                                                          flush_buf))
+            tw = time_launches(w, args.steps, args.warmup, torch, tkg, None, args.l2, flush_buf)
+            if fmt != "bf16" and not args.no_vendor_peak:
+                try:
+                    tv = time_launches(VendorGemm(w, torch), args.steps, args.warmup, torch, tkg, None, args.l2,
+                                       flush_buf)
+                    vendor_peak[fmt] = w.flop / tv / 1e12
+                except Exception:   # a vendor build without the format: no measured peak
+                    pass
+            by_format[fmt] = fmt_entry(w, tw)
             if w.fp32 is not None:
                 quant = quant_timings(w.fp32, 20, 3, torch, tkg, pk["hbm_gbs"])
             del w
@@ -751,6 +824,13 @@ def run_ours(args):
                 t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
                 sweep_scaled[f"{fmt} {s}"] = {"tflops": w.flop / t / 1e12, "us": t * 1e6, "input_groups": w.groups,
                                               "frac_of_pages_peak": w.flop / t / 1e12 / PAGES_PEAK_TFLOPS[fmt]}
+                del w
+                torch.cuda.empty_cache()
+        for fmt in ("bf16", "nvfp4"):
+            for s_ in [int(x) for x in args.nontile.split(",") if x]:
+                w = Workload(fmt, s_, SEEDS[fmt], l2, torch, tkg, synth)
+                t = time_launches(w, args.steps, min(args.warmup, 500), torch, tkg, None, args.l2, flush_buf)
+                nontile[f"{fmt} {s_}"] = fmt_entry(w, t)
                 del w
                 torch.cuda.empty_cache()
         for fmt in ("bf16", "nvfp4"):
@@ -810,7 +890,9 @@ def run_ours(args):
                          "frac": achieved / peak, "traffic": recorded_traffic(workload),
                          "peak_source": f"{pk['source']} cuBLAS bf16 burst x {NOMINAL_RATIO[hf]:g} (nominal {hf}/bf16)",
                          "frac_of_sustained": (achieved / (pk["bf16_sustained"] * NOMINAL_RATIO[hf])
-                                               if pk["bf16_sustained"] else None)},
+                                               if pk["bf16_sustained"] else None),
+                         "sustained": sustained,
+                         "configs": config_table(by_format, nontile, skinny, args.size)},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -818,6 +900,7 @@ def run_ours(args):
             "formats": by_format,
             "sweep_bf16": sweep,
             "sweep_scaled": sweep_scaled,
+            "nontile": nontile,
             "skinny": skinny,
             "quantize": quant,
             "grouped": grouped,
