@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtkg.so")
 SOURCES = ["tkg_api.cu", "quantize.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_nvfp4.cu", "gemm_noalloc.cu",
-           "gemm_grouped.cu", "host_pipeline.cu"]
+           "gemm_grouped.cu", "host_pipeline.cu", "gemm_list.cu"]
 HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "gemm_splitk.cuh", "host_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -165,8 +165,34 @@ struct GroupDev {
 struct NoGroups {
   int unused;
 };
+// A list of independent GEMMs in one launch (GROUPED == 3): GEMM e has its
+// own shape, operands, scales, output and alpha, given by its tensor maps and
+// the per-GEMM fields below; its output tiles are tile_start[e] ..
+// tile_start[e + 1] - 1 in the usual banded order.  Small GEMMs -- the
+// projections of one decode step, a batch of 512^3 products -- then share one
+// launch's fixed cost and fill the SMs together.
+constexpr int kMaxList = 16;
+struct GemmList {
+  CUtensorMap maps[kMaxList][5];      // A, B, SFA, SFB, D of each GEMM
+  int count;
+  int tile_start[kMaxList + 1];
+  int tiles_m[kMaxList];
+  int tiles_n[kMaxList];
+  int raster[kMaxList];               // M-blocks per raster band
+  int m[kMaxList];
+  int k[kMaxList];
+  int kstages[kMaxList];
+  int b_cta_rows[kMaxList];           // B rows each CTA of a pair supplies to one MMA
+  uint32_t tx_bytes[kMaxList];        // bytes per stage on the (leader's) full barrier
+  uint32_t idesc[kMaxList];           // MMA instruction descriptor (N narrowed for narrow GEMMs)
+  float alpha[kMaxList];
+  const float* ta[kMaxList];          // NVFP4 per-tensor scales (device, may be null)
+  const float* tb[kMaxList];
+};
 template <int GROUPED>
-using GroupArg = std::conditional_t<GROUPED == 1, GroupTable, std::conditional_t<GROUPED == 2, GroupDev, NoGroups>>;
+using GroupArg = std::conditional_t<
+    GROUPED == 1, GroupTable,
+    std::conditional_t<GROUPED == 2, GroupDev, std::conditional_t<GROUPED == 3, GemmList, NoGroups>>>;
 
 // Where one output tile's operands and results live.
 struct TileCoord {
@@ -290,7 +316,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
 }
 
 // GROUPED: 0 plain GEMM, 1 grouped with a host-built table, 2 grouped with
-// device-resident group sizes (static schedule only).
+// device-resident group sizes (static schedule only), 3 a list of GEMMs.
 template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC, int GROUPED = 0>
 __global__ void __launch_bounds__(384, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -355,10 +381,38 @@ __global__ void __launch_bounds__(384, 1)
     if constexpr (GROUPED == 2) return s_gtab[3 * kMaxGroups + 1 + g]; else if constexpr (GROUPED == 1) return gt.sfa_block0[g]; else return 0;
   };
 
+  constexpr bool kList = GROUPED == 3;
+  // tensor maps of the GEMM a tile belongs to (a list) or of the launch
+  auto map_a = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][0]; else { (void)e; return &tmA; } };
+  auto map_b = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][1]; else { (void)e; return &tmB; } };
+  auto map_sfa = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][2]; else { (void)e; return &tmSFA; } };
+  auto map_sfb = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][3]; else { (void)e; return &tmSFB; } };
+  auto map_d = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][4]; else { (void)e; return &tmD; } };
+  // per-GEMM K stages, K, MMA descriptor and stage bytes
+  auto kstages_of = [&](int e) { if constexpr (kList) return gt.kstages[e]; else { (void)e; return p.num_kstages; } };
+  auto k_of = [&](int e) { if constexpr (kList) return gt.k[e]; else { (void)e; return p.k; } };
+  auto idesc_of = [&](int e) { if constexpr (kList) return gt.idesc[e]; else { (void)e; return p.idesc; } };
+  auto tx_of = [&](int e) { if constexpr (kList) return gt.tx_bytes[e]; else { (void)e; return p.tx_bytes; } };
+
   // Tile t -> operand coordinates for this CTA.
   auto coords = [&](int t) {
     TileCoord tc;
-    if constexpr (GROUPED != 0) {
+    if constexpr (kList) {
+      int lo = 0, hi = gt.count;
+#pragma unroll 1
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (gt.tile_start[mid] <= t) lo = mid; else hi = mid;
+      }
+      const int e = lo;
+      tile_coords(t - gt.tile_start[e], gt.tiles_m[e], gt.tiles_n[e], gt.raster[e], tc.mb, tc.nb);
+      tc.a_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
+      tc.row_limit = gt.m[e];
+      tc.b_row = tc.nb * BN + int(rank) * gt.b_cta_rows[e];
+      tc.sfa_block = tc.a_row / 128;
+      tc.sfb_block0 = (tc.nb * BN) / 128;
+      tc.group = e;
+    } else if constexpr (GROUPED != 0) {
       // last group whose first tile is <= t (empty groups are skipped)
       int lo = 0, hi = gt.count;
 #pragma unroll 1
@@ -429,12 +483,12 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     if (GROUPED != 2 && ptx::elect_one() && int(blockIdx.x) / CG < p.num_tiles) {
       const TileCoord tc = coords(int(blockIdx.x) / CG);
-      const int npf = min(p.num_kstages, STAGES);
+      const int npf = min(kstages_of(tc.group), STAGES);
 #pragma unroll 1
       for (int ks = 0; ks < npf; ++ks) {
         const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
-        ptx::tma_prefetch_2d(&tmA, kx, tc.a_row);
-        ptx::tma_prefetch_2d(&tmB, kx, tc.b_row);
+        ptx::tma_prefetch_2d(map_a(tc.group), kx, tc.a_row);
+        ptx::tma_prefetch_2d(map_b(tc.group), kx, tc.b_row);
       }
     }
     __syncwarp();
@@ -570,13 +624,19 @@ __global__ void __launch_bounds__(384, 1)
         const int a_row = tc.a_row;
         const int b_row = tc.b_row;
         const int sfb_block0 = tc.sfb_block0;
+        const void* mA = map_a(tc.group);
+        const void* mB = map_b(tc.group);
+        const void* mSFA = map_sfa(tc.group);
+        const void* mSFB = map_sfb(tc.group);
+        const int nks = kstages_of(tc.group);
+        const uint32_t txb = tx_of(tc.group);
         // Serpentine K order: tiles of odd waves walk K backwards, so that they
         // start on the operand slices the previous wave read last, which are
         // still in L2 (BF16 16384^3: 13% fewer DRAM bytes).
         const bool rev = p.wave > 0 && ((t / p.wave) & 1);
 #pragma unroll 1
-        for (int it = 0; it < p.num_kstages; ++it) {
-          const int ks = rev ? p.num_kstages - 1 - it : it;
+        for (int it = 0; it < nks; ++it) {
+          const int ks = rev ? nks - 1 - it : it;
           if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, ctl)) {
             ok = false;
             break;
@@ -584,25 +644,25 @@ __global__ void __launch_bounds__(384, 1)
           armed &= ~(1u << stage);   // its previous load was consumed, hence complete
           const uint32_t fb = lead_full0 + 8u * stage;
           if (leader) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), p.tx_bytes);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), txb);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
           const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);   // TMA x coordinate (elements)
-          ptx::tma_load_2d<CG>(stage_a(stage), &tmA, kx, a_row, fb, pol_a);
-          ptx::tma_load_2d<CG>(stage_b(stage), &tmB, kx, b_row, fb, pol_b);
+          ptx::tma_load_2d<CG>(stage_a(stage), mA, kx, a_row, fb, pol_a);
+          ptx::tma_load_2d<CG>(stage_b(stage), mB, kx, b_row, fb, pol_b);
           if constexpr (C::kDual)   // second half of the 512-column tile
-            ptx::tma_load_2d<CG>(stage_b(stage) + uint32_t(C::kBBytes / 2), &tmB, kx, b_row + BN / 2, fb, pol_b);
+            ptx::tma_load_2d<CG>(stage_b(stage) + uint32_t(C::kBBytes / 2), mB, kx, b_row + BN / 2, fb, pol_b);
           if constexpr (C::kScaled) {
             const int atom0 = ks * T::kSfAtoms;
             // SFA: this CTA's 128 rows = scale block (a_row / 128)
-            ptx::tma_load_3d<CG>(stage_sfa(stage), &tmSFA, 0, atom0, tc.sfa_block, fb, pol_a);
+            ptx::tma_load_3d<CG>(stage_sfa(stage), mSFA, 0, atom0, tc.sfa_block, fb, pol_a);
             // SFB: every CTA of the pair holds the whole N tile's scales (the
             // MMA reads B scales from each CTA's tensor memory), so each CTA
             // loads every 128-row block itself; plain loads, no multicast.
 #pragma unroll
             for (int a = 0; a < C::kSfbBlocks; ++a)
-              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(a * T::kSfAtoms * 512), &tmSFB, 0, atom0,
+              ptx::tma_load_3d<CG>(stage_sfb(stage) + uint32_t(a * T::kSfAtoms * 512), mSFB, 0, atom0,
                                    sfb_block0 + a, fb, pol_b);
           }
           if (++stage == STAGES) {
@@ -644,9 +704,14 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(acc * C::kAccCols);
         const bool rev = p.wave > 0 && ((t / p.wave) & 1);   // the producer's K order
+        int e = 0;
+        if constexpr (kList) e = coords(t).group;
+        const int nks = kstages_of(e);
+        const int kk = k_of(e);
+        const uint32_t idesc0 = idesc_of(e);
 #pragma unroll 1
-        for (int it = 0; it < p.num_kstages; ++it) {
-          const int ks = rev ? p.num_kstages - 1 - it : it;
+        for (int it = 0; it < nks; ++it) {
+          const int ks = rev ? nks - 1 - it : it;
           if (!wait_bar<false>(full_bar(stage), phase, ctl)) {
             ok = false;
             break;
@@ -656,14 +721,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int j = 0; j < C::kMmasPerStage; ++j) {
             const int k0 = ks * T::kStageK + j * T::kMmaK;
-            if (k0 >= p.k) break;
+            if (k0 >= kk) break;
             const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
             const uint32_t accum = (it > 0 || j > 0) ? 1u : 0u;
             if constexpr (FMT == FMT_BF16) {
-              ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, p.idesc, accum);
+              ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, idesc0, accum);
               if constexpr (C::kDual) {
                 const uint64_t bdesc1 = sdesc_sw128(stage_b(stage) + uint32_t(C::kBBytes / 2));
-                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, p.idesc, accum);
+                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, idesc0, accum);
               }
             } else {
               // scales -> tensor memory from this thread, right before the MMAs that
@@ -680,12 +745,12 @@ __global__ void __launch_bounds__(384, 1)
               }
               const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
               if constexpr (FMT == FMT_MXFP8) {
-                const uint32_t idesc = p.idesc | (uint32_t(j) << 29) | (uint32_t(j) << 4);
+                const uint32_t idesc = idesc0 | (uint32_t(j) << 29) | (uint32_t(j) << 4);
                 ptx::mma_mxf8<CG>(d_tmem, adesc + koff, bdesc + koff, idesc, reg, reg + 4u, accum);
               } else {
-                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, p.idesc, reg, reg + 4u, accum);
+                ptx::mma_nvf4<CG>(d_tmem, adesc + koff, bdesc + koff, idesc0, reg, reg + 4u, accum);
               }
-              if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= p.k) {
+              if (FMT == FMT_NVFP4 || j == C::kMmasPerStage - 1 || k0 + T::kMmaK >= kk) {
                 if (++region == uint32_t(C::kRegions)) region = 0;
               }
             }
@@ -759,9 +824,15 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = first_tile; t >= 0;) {
       const TileCoord tc = coords(t);
       float alpha = alpha0;
-      if constexpr (GROUPED) {
+      if constexpr (GROUPED == 1 || GROUPED == 2) {
         if (gt.tb) alpha = alpha * __ldg(gt.tb + tc.group);
+      } else if constexpr (kList) {
+        // fp32(fp32(alpha * tA) * tB), as for the single GEMM
+        alpha = gt.alpha[tc.group];
+        if (gt.ta[tc.group]) alpha = alpha * __ldg(gt.ta[tc.group]);
+        if (gt.tb[tc.group]) alpha = alpha * __ldg(gt.tb[tc.group]);
       }
+      const void* mD = map_d(tc.group);
       // All 32 lanes wait, converged.  The issuing roles above run in one
       // elected lane (a producer or MMA warp whose 32 lanes ran the loop, with
       // one lane issuing, measured 5% and 2x slower on NVFP4), but eight
@@ -772,7 +843,7 @@ __global__ void __launch_bounds__(384, 1)
       const int row0 = tc.a_row + q * 32;
       // a 32-row box that crosses the end of a group (grouped GEMM) is stored
       // row by row so that the next group's rows are left alone
-      const bool masked = GROUPED && row0 + 32 > tc.row_limit;
+      const bool masked = (GROUPED == 1 || GROUPED == 2) && row0 + 32 > tc.row_limit;
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
 #pragma unroll
       for (int pass = 0; pass < kPasses; ++pass) {
@@ -807,7 +878,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         const int col0 = tc.nb * BN + h * (BN / 2) + pass * 128;
         if (masked) {
-          if constexpr (GROUPED) {
+          if constexpr (GROUPED == 1 || GROUPED == 2) {
             const int r = row0 + lane;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -856,7 +927,7 @@ __global__ void __launch_bounds__(384, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_2d(&tmD, buf, col0 + c * 32, row0);
+            ptx::tma_store_2d(mD, buf, col0 + c * 32, row0);
             ptx::bulk_commit_group();
           }
         }

@@ -31,7 +31,18 @@ EXPORTS = [
     "tkg_gemm_grouped_bf16", "tkg_gemm_grouped_mxfp8", "tkg_gemm_grouped_nvfp4", "tkg_grouped_scale_bytes",
     "tkg_gemm_bf16_from_host", "tkg_gemm_grouped_dev_bf16", "tkg_gemm_grouped_dev_mxfp8",
     "tkg_gemm_grouped_dev_nvfp4", "tkg_grouped_dev_scale_bytes", "tkg_quantize_nvfp4_scaled",
+    "tkg_gemm_list_bf16", "tkg_gemm_list_mxfp8", "tkg_gemm_list_nvfp4",
 ]
+
+MAX_LIST = 16
+
+
+class GemmDesc(ctypes.Structure):
+    """tkg_gemm_desc: one GEMM of a list (device pointers, sizes, alpha)."""
+    _fields_ = [("m", ctypes.c_int), ("n", ctypes.c_int), ("k", ctypes.c_int),
+                ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("sfa", ctypes.c_void_p), ("sfb", ctypes.c_void_p),
+                ("tensor_scale_a", ctypes.c_void_p), ("tensor_scale_b", ctypes.c_void_p),
+                ("D", ctypes.c_void_p), ("alpha", ctypes.c_float)]
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +81,9 @@ def load() -> ctypes.CDLL:
             lib.tkg_gemm_grouped_dev_nvfp4.argtypes = [i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp]
             lib.tkg_grouped_dev_scale_bytes.argtypes = [i, i, i, i]
             lib.tkg_grouped_dev_scale_bytes.restype = ctypes.c_size_t
+            for name in ("tkg_gemm_list_bf16", "tkg_gemm_list_mxfp8", "tkg_gemm_list_nvfp4"):
+                getattr(lib, name).argtypes = [i, ctypes.POINTER(GemmDesc), vp]
+                getattr(lib, name).restype = ctypes.c_int
             lib.tkg_get_device_status.argtypes = [vp]
             lib.tkg_status_string.argtypes = [st]
             lib.tkg_status_string.restype = ctypes.c_char_p
@@ -242,6 +256,25 @@ def gemm_grouped_dev_nvfp4(sizes_dev, A, B, sfa, sfb, D, alpha: float = 1.0, ta=
     _check(load().tkg_gemm_grouped_dev_nvfp4(g, _ptr(sizes_dev), A.shape[0], B.shape[-2], 2 * A.shape[-1], _ptr(A),
                                              _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
                                              ctypes.c_float(alpha), _stream(stream)), "tkg_gemm_grouped_dev_nvfp4")
+
+
+def gemm_list_raw(fmt: str, descs, stream) -> int:
+    """tkg_gemm_list_<fmt> on a sequence of GemmDesc."""
+    arr = (GemmDesc * max(len(descs), 1))(*descs)
+    return getattr(load(), f"tkg_gemm_list_{fmt}")(len(descs), arr, stream)
+
+
+def gemm_desc(fmt: str, A, B, D, alpha: float = 1.0, sfa=None, sfb=None, ta=None, tb=None) -> GemmDesc:
+    """Descriptor of one GEMM from its device tensors (A: m x k, or m x k/2 bytes for NVFP4)."""
+    m = A.shape[0]
+    k = 2 * A.shape[1] if fmt == "nvfp4" else A.shape[1]
+    return GemmDesc(m, B.shape[0], k, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
+                    float(alpha))
+
+
+def gemm_list(fmt: str, descs, stream=None) -> None:
+    """Several independent GEMMs (GemmDesc each, at most MAX_LIST) in one launch."""
+    _check(gemm_list_raw(fmt, descs, _stream(stream)), f"tkg_gemm_list_{fmt}")
 
 
 def grouped_dev_scale_bytes(groups: int, m_capacity: int, k: int, block: int) -> int:

@@ -152,6 +152,37 @@ tkg_status tkg_gemm_grouped_dev_nvfp4(int groups, const int *m_sizes_dev, int m_
  * groups * tkg_scale_bytes(128, k, block).  0 for invalid arguments. */
 size_t tkg_grouped_dev_scale_bytes(int groups, int m_capacity, int k, int block);
 
+/* A list of independent GEMMs run by one persistent launch ("ThunderKittens
+ * 2.0 GPU Kernel优化", table of updates: cluster-launch-control scheduling and
+ * programmatic dependent launch, named there as the means for back-to-back
+ * small GEMMs).  Each entry is a whole GEMM of its own, with the plain
+ * entry point's product, layouts and requirements for its format:
+ *   D_e = bf16_rn(alpha_e' * A_e * B_e^T),  A_e: m x k, B_e: n x k, D_e: m x n,
+ * alpha_e' = alpha (BF16, MXFP8) or fp32(fp32(alpha * tA) * tB) (NVFP4, either
+ * pointer may be NULL meaning 1.0).  All entries' output tiles form one tile
+ * list, so small GEMMs -- the projections of one decode step, a batch of
+ * 512^3 products -- fill the SMs together and pay one launch's fixed cost.
+ *  - gemms: HOST array of `count` descriptors (1..16), read during the call.
+ *    Entries with m == 0 or n == 0 are skipped; k == 0 writes zeros to D.
+ *  - sfa / sfb: tiled scales as in tkg_gemm_mxfp8 / tkg_gemm_nvfp4 (ignored
+ *    for BF16); tensor_scale_a / tensor_scale_b: NVFP4 only.
+ *  - The outputs must not overlap one another or any entry's inputs.
+ * Errors: count outside 1..16 or gemms NULL -> TKG_ERR_INVALID_ARG
+ * (count > 16: TKG_ERR_UNSUPPORTED); an entry failing the plain entry point's
+ * checks -> that entry point's error, and nothing is launched. */
+typedef struct {
+  int m, n, k;
+  const void *A, *B;
+  const void *sfa, *sfb;
+  const float *tensor_scale_a, *tensor_scale_b;
+  void *D;
+  float alpha;
+} tkg_gemm_desc;
+
+tkg_status tkg_gemm_list_bf16(int count, const tkg_gemm_desc *gemms, cudaStream_t stream);
+tkg_status tkg_gemm_list_mxfp8(int count, const tkg_gemm_desc *gemms, cudaStream_t stream);
+tkg_status tkg_gemm_list_nvfp4(int count, const tkg_gemm_desc *gemms, cudaStream_t stream);
+
 /* BF16 GEMM on operands in HOST memory (the same product as tkg_gemm_bf16;
  * no counterpart on the pages, which time device-resident GEMMs only).
  * A_host (m x k), B_host (n x k): bfloat16, row-major, read; D_host (m x n):

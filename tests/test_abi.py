@@ -118,3 +118,25 @@ def test_grouped_dev_host_checks():
     assert lib.tkg_gemm_grouped_dev_bf16(2, fake, 8, 8, 0, None, None, None, f, None) == tkg.ERR_UNSUPPORTED
     assert tkg.grouped_dev_scale_bytes(4, 1000, 256, 16) == \
         tkg.scale_bytes(1000, 256, 16) + 4 * tkg.scale_bytes(128, 256, 16)
+
+
+def test_gemm_list_host_side_checks(lib):
+    # every entry is checked before anything is launched; no CUDA call is made
+    from dense_block_scaled_gb300 import tkg
+    assert ctypes.sizeof(tkg.GemmDesc) == 80   # the C struct: 3 ints, 7 pointers, a float, padding
+    ok = tkg.GemmDesc(64, 64, 64, 16, 16, 16, 16, None, None, 16, 1.0)
+    assert tkg.gemm_list_raw("bf16", [], None) == tkg.ERR_INVALID_ARG
+    assert tkg.gemm_list_raw("bf16", [ok] * (tkg.MAX_LIST + 1), None) == tkg.ERR_UNSUPPORTED
+    bad_m = tkg.GemmDesc(-1, 64, 64, 16, 16, 16, 16, None, None, 16, 1.0)
+    assert tkg.gemm_list_raw("bf16", [ok, bad_m], None) == tkg.ERR_INVALID_ARG
+    bad_n = tkg.GemmDesc(64, 12, 64, 16, 16, 16, 16, None, None, 16, 1.0)
+    assert tkg.gemm_list_raw("mxfp8", [ok, bad_n], None) == tkg.ERR_ALIGNMENT
+    bad_k = tkg.GemmDesc(64, 64, 48, 16, 16, 16, 16, None, None, 16, 1.0)
+    assert tkg.gemm_list_raw("nvfp4", [bad_k, ok], None) == tkg.ERR_ALIGNMENT
+    no_scales = tkg.GemmDesc(64, 64, 64, 16, 16, None, 16, None, None, 16, 1.0)
+    assert tkg.gemm_list_raw("mxfp8", [ok, no_scales], None) == tkg.ERR_INVALID_ARG
+    bad_ta = tkg.GemmDesc(64, 64, 64, 16, 16, 16, 16, 18, None, 16, 1.0)
+    assert tkg.gemm_list_raw("nvfp4", [ok, bad_ta], None) == tkg.ERR_ALIGNMENT
+    # empty entries only: nothing to do
+    empty = tkg.GemmDesc(0, 64, 64, None, None, None, None, None, None, None, 1.0)
+    assert tkg.gemm_list_raw("bf16", [empty, empty], None) == tkg.OK
