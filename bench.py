@@ -61,6 +61,7 @@ def parse_args():
                     help="M values of the skinny N=K=8192 GEMMs reported (1: batch-1 decode)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-list", action="store_true", help="skip the GEMM-list timings")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantiser timings")
     ap.add_argument("--grouped-decode", default="8,16,4096,7168",
                     help="experts,rows per expert,N,K of the decode-regime grouped GEMM (empty: skip)")
@@ -318,6 +319,66 @@ def grouped_sizes(groups, total, seed=GROUPED_SEED):
     import numpy as np
     rng = np.random.default_rng(seed)
     return [int(x) * 128 for x in rng.multinomial(total // 128, [1.0 / groups] * groups)]
+
+
+LIST_CASES = [
+    # label, format, shapes: independent GEMMs (own operands each) in one tkg_gemm_list_* launch
+    ("BF16 8 x 512^3", "bf16", [(512, 512, 512)] * 8),
+    ("BF16 8 x M=16 N=K=8192", "bf16", [(16, 8192, 8192)] * 8),
+    ("NVFP4 8 x M=16 N=K=8192", "nvfp4", [(16, 8192, 8192)] * 8),
+]
+LIST_SEED = 1100
+
+
+class ListWorkload:
+    """Several independent GEMMs (seeded N(0,1) operands each; block-scaled ones
+    quantised by the library's quantisers) run as one tkg_gemm_list launch, in
+    identical copies rotated so that every launch reads cold L2."""
+
+    def __init__(self, fmt, shapes, seed, l2_bytes, torch, tkg, synth):
+        self.fmt, self.shapes = fmt, shapes
+        dev = torch.device("cuda")
+        base = []
+        for i, (m, n, k) in enumerate(shapes):
+            w = Workload(fmt, 0, seed + i, 0, torch, tkg, synth, mnk=(m, n, k))   # one copy (no rotation)
+            base.append(w.sets[0] + [w.D[0]])
+            del w
+        self.in_bytes = sum(int(o.numel() * o.element_size()) for ops in base for o in ops[:6] if o is not None)
+        self.out_bytes = sum(m * n * 2 for m, n, _ in shapes)
+        self.groups = 1 if self.in_bytes >= 3 * l2_bytes else (3 * l2_bytes) // self.in_bytes + 1
+        self.sets = [base] + [[[o.clone() if o is not None else None for o in ops] for ops in base]
+                              for _ in range(self.groups - 1)]
+        self.descs = []
+        for st in self.sets:
+            self.descs.append([tkg.gemm_desc(fmt, A, B, D, 1.0, sfa=sa, sfb=sb, ta=ta, tb=tb)
+                               for A, B, sa, sb, ta, tb, D in st])
+        self.flop = sum(2.0 * m * n * k for m, n, k in shapes)
+        del dev
+
+    def launch(self, i, tkg):
+        tkg.gemm_list(self.fmt, self.descs[i % self.groups])
+
+
+def list_timings(steps, warmup, l2, torch, tkg, synth, hbm_gbs, single):
+    """Per case: time per list launch, per GEMM, TFLOP/s and the fraction of the
+    HBM roofline over all operand and output bytes; `single` gives the same
+    GEMM's one-launch time where the bench measured it."""
+    out = {}
+    for label, fmt, shapes in LIST_CASES:
+        w = ListWorkload(fmt, shapes, LIST_SEED, l2, torch, tkg, synth)
+        t = time_launches(w, steps, warmup, torch, tkg)
+        byts = w.in_bytes + w.out_bytes
+        e = {"us_per_launch": t * 1e6, "us_per_gemm": t * 1e6 / len(shapes), "tflops": w.flop / t / 1e12,
+             "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs, "gemms": len(shapes),
+             "input_groups": w.groups}
+        one = single.get(label)
+        if one:
+            e["single_launch_us"] = one
+            e["speedup_vs_single_launches"] = one * len(shapes) / (t * 1e6)
+        out[label] = e
+        del w
+        torch.cuda.empty_cache()
+    return out
 
 
 def grouped_timings(formats, groups, total, n, k, steps, warmup, torch, tkg, synth):
@@ -649,7 +710,7 @@ def l2_description(groups, mode):
     return "inputs larger than 3x L2, no rotation needed" if groups == 1 else f"{groups} rotated input groups"
 
 
-def config_table(by_format, nontile, skinny, size):
+def config_table(by_format, nontile, skinny, size, lists=None):
     """The workload definition's configurations in one compact table (TFLOP/s or
     microseconds and the roofline fractions), for the headline line's roofline
     object."""
@@ -667,6 +728,9 @@ def config_table(by_format, nontile, skinny, size):
         out[key.replace("bf16", "BF16").replace("nvfp4", "NVFP4")] = {
             "us": e["us"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
             "frac_of_roofline": e["frac_of_roofline"]}
+    for key, e in (lists or {}).items():
+        out["list " + key] = {"us_per_gemm": e["us_per_gemm"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
+                              "speedup_vs_single_launches": e.get("speedup_vs_single_launches")}
     return out
 
 
@@ -787,6 +851,7 @@ def run_ours(args):
 
     by_format, sweep, sweep_scaled, skinny, quant, grouped, grouped_decode = {}, {}, {}, {}, {}, {}, {}
     nontile = {}
+    lists = {}
     vendor = {}
     e2e = None
     if rank == 0:
@@ -847,6 +912,12 @@ def run_ours(args):
                     "us_graph": tg * 1e6, "frac_of_roofline_graph": w.flop / tg / 1e12 / roof}
                 del w
                 torch.cuda.empty_cache()
+        if not args.no_list:
+            single = {"BF16 8 x 512^3": sweep.get("512", {}).get("us"),
+                      "BF16 8 x M=16 N=K=8192": skinny.get("bf16 M=16 N=K=8192", {}).get("us"),
+                      "NVFP4 8 x M=16 N=K=8192": skinny.get("nvfp4 M=16 N=K=8192", {}).get("us")}
+            lists = list_timings(max(args.steps, 100), min(args.warmup, 50), l2, torch, tkg, synth, pk["hbm_gbs"],
+                                 single)
         if args.grouped:
             gg, gt, gn, gk = [int(x) for x in args.grouped.split(",")]
             grouped = grouped_timings([f for f in ("bf16", "mxfp8", "nvfp4")], gg, gt, gn, gk,
@@ -892,7 +963,7 @@ def run_ours(args):
                          "frac_of_sustained": (achieved / (pk["bf16_sustained"] * NOMINAL_RATIO[hf])
                                                if pk["bf16_sustained"] else None),
                          "sustained": sustained,
-                         "configs": config_table(by_format, nontile, skinny, args.size)},
+                         "configs": config_table(by_format, nontile, skinny, args.size, lists)},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -901,6 +972,7 @@ def run_ours(args):
             "sweep_bf16": sweep,
             "sweep_scaled": sweep_scaled,
             "nontile": nontile,
+            "gemm_list": lists,
             "skinny": skinny,
             "quantize": quant,
             "grouped": grouped,
