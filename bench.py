@@ -371,10 +371,17 @@ def list_timings(steps, warmup, l2, torch, tkg, synth, hbm_gbs, single):
         e = {"us_per_launch": t * 1e6, "us_per_gemm": t * 1e6 / len(shapes), "tflops": w.flop / t / 1e12,
              "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs, "gemms": len(shapes),
              "input_groups": w.groups}
-        one = single.get(label)
+        tg = graph_seconds(w, steps, torch, tkg)
+        e["us_per_launch_graph"] = tg * 1e6
+        e["us_per_gemm_graph"] = tg * 1e6 / len(shapes)
+        e["frac_of_hbm_graph"] = byts / tg / 1e9 / hbm_gbs
+        one, one_graph = single.get(label, (None, None))
         if one:
             e["single_launch_us"] = one
             e["speedup_vs_single_launches"] = one * len(shapes) / (t * 1e6)
+        if one_graph:
+            e["single_launch_us_graph"] = one_graph
+            e["speedup_vs_single_launches_graph"] = one_graph * len(shapes) / (tg * 1e6)
         out[label] = e
         del w
         torch.cuda.empty_cache()
@@ -730,7 +737,9 @@ def config_table(by_format, nontile, skinny, size, lists=None):
             "frac_of_roofline": e["frac_of_roofline"]}
     for key, e in (lists or {}).items():
         out["list " + key] = {"us_per_gemm": e["us_per_gemm"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
-                              "speedup_vs_single_launches": e.get("speedup_vs_single_launches")}
+                              "speedup_vs_single_launches": e.get("speedup_vs_single_launches"),
+                              "us_per_gemm_graph": e.get("us_per_gemm_graph"),
+                              "speedup_vs_single_launches_graph": e.get("speedup_vs_single_launches_graph")}
     return out
 
 
@@ -913,9 +922,11 @@ def run_ours(args):
                 del w
                 torch.cuda.empty_cache()
         if not args.no_list:
-            single = {"BF16 8 x 512^3": sweep.get("512", {}).get("us"),
-                      "BF16 8 x M=16 N=K=8192": skinny.get("bf16 M=16 N=K=8192", {}).get("us"),
-                      "NVFP4 8 x M=16 N=K=8192": skinny.get("nvfp4 M=16 N=K=8192", {}).get("us")}
+            def us(d):
+                return (d.get("us"), d.get("us_graph")) if d else (None, None)
+            single = {"BF16 8 x 512^3": us(sweep.get("512")),
+                      "BF16 8 x M=16 N=K=8192": us(skinny.get("bf16 M=16 N=K=8192")),
+                      "NVFP4 8 x M=16 N=K=8192": us(skinny.get("nvfp4 M=16 N=K=8192"))}
             lists = list_timings(max(args.steps, 100), min(args.warmup, 50), l2, torch, tkg, synth, pk["hbm_gbs"],
                                  single)
         if args.grouped:

@@ -48,7 +48,7 @@ template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED>
 tkg_status launch_list(const tkg_gemm_desc* const* gemms, int count, cudaStream_t stream) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
-  static_assert(!C::kDual, "lists run 256-column tiles");
+  static_assert(!C::kDual, "lists run 128- or 256-column tiles");
   auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC, SCHED, 3>;
   constexpr int kLaunchSmem = C::kSmemBytes > 118784 ? C::kSmemBytes : 118784;   // one CTA per SM
 
@@ -198,18 +198,23 @@ tkg_status launch_list_sched(const tkg_gemm_desc* const* gemms, int count, cudaS
   return launch_list<FMT, CG, BN, STAGES, ACC, SCHED_CLC>(gemms, count, s);
 }
 
-// Single-CTA tiles (128 x 256) unless the list has at least one wave of
-// 256 x 256 pair tiles: below that, pairs leave as many SMs idle as single
-// tiles do and gain nothing from sharing B.
-bool list_single_cta(const tkg_gemm_desc* const* gemms, int count) {
+// Tile shape of a list: 256 x 256 CTA pairs when the list has at least one
+// wave of them; else single-CTA 128 x 256 tiles (pairs would leave as many SMs
+// idle and gain nothing from sharing B); and 128 x 128 single-CTA tiles when
+// even twice as many of those still fit one wave (a batch of 512^3 GEMMs: the
+// narrower tiles put twice the SMs to work on the same FLOPs).
+enum ListTiles { kPair256, kSingle256, kSingle128 };
+ListTiles list_tiles(const tkg_gemm_desc* const* gemms, int count) {
   const int cg = option(TKG_OPT_CTA_GROUP);
-  if (cg != 0) return cg == 1;
   int sms = 0;
-  if (device_sm_count(&sms) != TKG_OK) return true;
-  long long pair_tiles = 0;
-  for (int e = 0; e < count; ++e)
+  if (device_sm_count(&sms) != TKG_OK) sms = 148;
+  long long pair_tiles = 0, single_tiles = 0;
+  for (int e = 0; e < count; ++e) {
     pair_tiles += (long long)ceil_div(gemms[e]->m, 256) * ceil_div(gemms[e]->n, 256);
-  return pair_tiles < sms / 2;
+    single_tiles += (long long)ceil_div(gemms[e]->m, 128) * ceil_div(gemms[e]->n, 256);
+  }
+  if (cg == 2 || (cg == 0 && pair_tiles >= sms / 2)) return kPair256;
+  return 2 * single_tiles <= sms ? kSingle128 : kSingle256;
 }
 
 tkg_status gemm_list(int fmt, int count, const tkg_gemm_desc* gemms, cudaStream_t stream) {
@@ -229,16 +234,19 @@ tkg_status gemm_list(int fmt, int count, const tkg_gemm_desc* gemms, cudaStream_
     if (zero[e] && cudaMemsetAsync(gemms[e].D, 0, size_t(gemms[e].m) * size_t(gemms[e].n) * 2, stream) != cudaSuccess)
       return TKG_ERR_CUDA;
   if (nrun == 0) return TKG_OK;
-  const bool single = list_single_cta(run, nrun);
+  const ListTiles tiles = list_tiles(run, nrun);
   if (fmt == FMT_BF16) {
-    if (single) return launch_list_sched<FMT_BF16, 1, 256, 4, 2>(run, nrun, stream);
+    if (tiles == kSingle128) return launch_list_sched<FMT_BF16, 1, 128, 6, 2>(run, nrun, stream);
+    if (tiles == kSingle256) return launch_list_sched<FMT_BF16, 1, 256, 4, 2>(run, nrun, stream);
     return launch_list_sched<FMT_BF16, 2, 256, 6, 2>(run, nrun, stream);
   }
   if (fmt == FMT_MXFP8) {
-    if (single) return launch_list_sched<FMT_MXFP8, 1, 256, 4, 1>(run, nrun, stream);
+    if (tiles == kSingle128) return launch_list_sched<FMT_MXFP8, 1, 128, 6, 1>(run, nrun, stream);
+    if (tiles == kSingle256) return launch_list_sched<FMT_MXFP8, 1, 256, 4, 1>(run, nrun, stream);
     return launch_list_sched<FMT_MXFP8, 2, 256, 6, 1>(run, nrun, stream);
   }
-  if (single) return launch_list_sched<FMT_NVFP4, 1, 256, 3, 1>(run, nrun, stream);
+  if (tiles == kSingle128) return launch_list_sched<FMT_NVFP4, 1, 128, 5, 1>(run, nrun, stream);
+  if (tiles == kSingle256) return launch_list_sched<FMT_NVFP4, 1, 256, 3, 1>(run, nrun, stream);
   return launch_list_sched<FMT_NVFP4, 2, 256, 5, 1>(run, nrun, stream);
 }
 
