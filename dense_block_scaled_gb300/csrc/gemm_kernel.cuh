@@ -67,6 +67,13 @@ struct GemmParams {
                              // may be shorter than the tile (rows past them feed only unstored results)
   uint32_t idesc;            // MMA instruction descriptor (N may be narrower than the tile for narrow B)
   int b_cta_rows;            // B rows each CTA of the pair supplies to one MMA
+  // Half-width tiles (plain GEMMs): tiles at or past tail_start are halves of
+  // the last original tiles, two per tile (the last partial wave, split so it
+  // runs in about half the time); tail_start == num_tiles when there are none.
+  int tail_start;
+  uint32_t tx_half;          // stage bytes of a half tile
+  uint32_t idesc_half;       // its MMA descriptor (N halved; dual accumulate: one of its two MMAs)
+  int b_cta_rows_half;       // B rows each CTA supplies to a half tile's MMA
 };
 
 template <int FMT>
@@ -196,6 +203,8 @@ using GroupArg = std::conditional_t<
 
 // Where one output tile's operands and results live.
 struct TileCoord {
+  int half;          // -1: a whole tile; 0 / 1: the first or second half (columns) of one
+  int n0;            // first column of the tile (or half)
   int mb, nb;        // M-block (of kMmaM rows) and N-block of the tile
   int a_row;         // first row of this CTA's A rows (and D rows)
   int row_limit;     // rows at or past this one are not stored
@@ -321,7 +330,8 @@ template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC
 __global__ void __launch_bounds__(384, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                const __grid_constant__ CUtensorMap tmD, const GemmParams p, const __grid_constant__ GroupArg<GROUPED> gt) {
+                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmBh, const GemmParams p,
+                const __grid_constant__ GroupArg<GROUPED> gt) {
   using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
@@ -412,6 +422,8 @@ __global__ void __launch_bounds__(384, 1)
       tc.sfa_block = tc.a_row / 128;
       tc.sfb_block0 = (tc.nb * BN) / 128;
       tc.group = e;
+      tc.half = -1;
+      tc.n0 = tc.nb * BN;
     } else if constexpr (GROUPED != 0) {
       // last group whose first tile is <= t (empty groups are skipped)
       int lo = 0, hi = gt.count;
@@ -431,13 +443,24 @@ __global__ void __launch_bounds__(384, 1)
       tc.sfa_block = tab_sfa0(g) + local_row / 128;
       tc.sfb_block0 = g * gt.n_blocks + (tc.nb * BN) / 128;
       tc.group = g;
+      tc.half = -1;
+      tc.n0 = tc.nb * BN;
     } else {
-      tile_coords(t, p.tiles_m, p.tiles_n, p.raster_group, tc.mb, tc.nb);
+      // tiles past tail_start are halves of the last tiles: tile tail_start + u / 2, half u % 2
+      int o = t;
+      tc.half = -1;
+      if (t >= p.tail_start) {
+        const int u = t - p.tail_start;
+        o = p.tail_start + (u >> 1);
+        tc.half = u & 1;
+      }
+      tile_coords(o, p.tiles_m, p.tiles_n, p.raster_group, tc.mb, tc.nb);
+      tc.n0 = tc.nb * BN + (tc.half > 0 ? BN / 2 : 0);
       tc.a_row = tc.mb * C::kMmaM + int(rank) * C::kCtaM;
       tc.row_limit = p.m;
-      tc.b_row = tc.nb * BN + int(rank) * p.b_cta_rows;
+      tc.b_row = tc.n0 + int(rank) * (tc.half >= 0 ? p.b_cta_rows_half : p.b_cta_rows);
       tc.sfa_block = tc.a_row / 128;
-      tc.sfb_block0 = (tc.nb * BN) / 128;
+      tc.sfb_block0 = tc.n0 / 128;
       tc.group = 0;
     }
     return tc;
@@ -625,11 +648,14 @@ __global__ void __launch_bounds__(384, 1)
         const int b_row = tc.b_row;
         const int sfb_block0 = tc.sfb_block0;
         const void* mA = map_a(tc.group);
-        const void* mB = map_b(tc.group);
+        const bool half = tc.half >= 0;
+        // a half tile's B box: half the rows per CTA (a second map), or for dual
+        // accumulate one of its two boxes
+        const void* mB = (half && !C::kDual) ? static_cast<const void*>(&tmBh) : map_b(tc.group);
         const void* mSFA = map_sfa(tc.group);
         const void* mSFB = map_sfb(tc.group);
         const int nks = kstages_of(tc.group);
-        const uint32_t txb = tx_of(tc.group);
+        const uint32_t txb = half ? p.tx_half : tx_of(tc.group);
         // Serpentine K order: tiles of odd waves walk K backwards, so that they
         // start on the operand slices the previous wave read last, which are
         // still in L2 (BF16 16384^3: 13% fewer DRAM bytes).
@@ -651,8 +677,10 @@ __global__ void __launch_bounds__(384, 1)
           const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);   // TMA x coordinate (elements)
           ptx::tma_load_2d<CG>(stage_a(stage), mA, kx, a_row, fb, pol_a);
           ptx::tma_load_2d<CG>(stage_b(stage), mB, kx, b_row, fb, pol_b);
-          if constexpr (C::kDual)   // second half of the 512-column tile
-            ptx::tma_load_2d<CG>(stage_b(stage) + uint32_t(C::kBBytes / 2), mB, kx, b_row + BN / 2, fb, pol_b);
+          if constexpr (C::kDual) {   // second half of the 512-column tile
+            if (!half)
+              ptx::tma_load_2d<CG>(stage_b(stage) + uint32_t(C::kBBytes / 2), mB, kx, b_row + BN / 2, fb, pol_b);
+          }
           if constexpr (C::kScaled) {
             const int atom0 = ks * T::kSfAtoms;
             // SFA: this CTA's 128 rows = scale block (a_row / 128)
@@ -705,10 +733,15 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t d_tmem = tmem + uint32_t(acc * C::kAccCols);
         const bool rev = p.wave > 0 && ((t / p.wave) & 1);   // the producer's K order
         int e = 0;
-        if constexpr (kList) e = coords(t).group;
+        bool half = false;
+        if constexpr (kList) {
+          e = coords(t).group;
+        } else if constexpr (GROUPED == 0) {
+          half = t >= p.tail_start;
+        }
         const int nks = kstages_of(e);
         const int kk = k_of(e);
-        const uint32_t idesc0 = idesc_of(e);
+        const uint32_t idesc0 = half ? p.idesc_half : idesc_of(e);
 #pragma unroll 1
         for (int it = 0; it < nks; ++it) {
           const int ks = rev ? nks - 1 - it : it;
@@ -727,8 +760,10 @@ __global__ void __launch_bounds__(384, 1)
             if constexpr (FMT == FMT_BF16) {
               ptx::mma_f16<CG>(d_tmem, adesc + koff, bdesc + koff, idesc0, accum);
               if constexpr (C::kDual) {
-                const uint64_t bdesc1 = sdesc_sw128(stage_b(stage) + uint32_t(C::kBBytes / 2));
-                ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, idesc0, accum);
+                if (!half) {
+                  const uint64_t bdesc1 = sdesc_sw128(stage_b(stage) + uint32_t(C::kBBytes / 2));
+                  ptx::mma_f16<CG>(d_tmem + 256u, adesc + koff, bdesc1 + koff, idesc0, accum);
+                }
               }
             } else {
               // scales -> tensor memory from this thread, right before the MMAs that
@@ -845,13 +880,16 @@ __global__ void __launch_bounds__(384, 1)
       // row by row so that the next group's rows are left alone
       const bool masked = (GROUPED == 1 || GROUPED == 2) && row0 + 32 > tc.row_limit;
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
+      // a half tile holds BN / 2 columns: the warps of the second column half
+      // only hand the accumulator back
+      const bool idle = tc.half >= 0 && h == 1;
 #pragma unroll
       for (int pass = 0; pass < kPasses; ++pass) {
         const int nch = kWarpChunks - 4 * pass < 4 ? kWarpChunks - 4 * pass : 4;
         uint32_t v[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          if (c < nch) ptx::tmem_ld_32x32b_x32(tbase + uint32_t(pass * 128 + c * 32), v[c]);
+          if (c < nch && !idle) ptx::tmem_ld_32x32b_x32(tbase + uint32_t(pass * 128 + c * 32), v[c]);
         ptx::tmem_ld_wait();
         if (pass == kPasses - 1) {
           ptx::tc_fence_before();
@@ -876,7 +914,8 @@ __global__ void __launch_bounds__(384, 1)
             accph ^= 1u;
           }
         }
-        const int col0 = tc.nb * BN + h * (BN / 2) + pass * 128;
+        if (idle) continue;
+        const int col0 = tc.n0 + h * (BN / 2) + pass * 128;
         if (masked) {
           if constexpr (GROUPED == 1 || GROUPED == 2) {
             const int r = row0 + lane;

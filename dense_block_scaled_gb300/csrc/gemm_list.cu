@@ -123,6 +123,7 @@ tkg_status launch_list(const tkg_gemm_desc* const* gemms, int count, cudaStream_
 
   GemmParams p{};
   p.num_tiles = int(tiles);
+  p.tail_start = p.num_tiles;   // lists keep whole tiles
   p.alpha = 1.0f;
   p.ta = nullptr;
   p.tb = nullptr;
@@ -184,7 +185,8 @@ tkg_status launch_list(const tkg_gemm_desc* const* gemms, int count, cudaStream_
   cfg.gridDim = dim3(clusters * CG, 1, 1);
   p.wave = max_clusters;
   cudaError_t err =
-      cudaLaunchKernelEx(&cfg, kern, gl.maps[0][0], gl.maps[0][1], gl.maps[0][2], gl.maps[0][3], gl.maps[0][4], p, gl);
+      cudaLaunchKernelEx(&cfg, kern, gl.maps[0][0], gl.maps[0][1], gl.maps[0][2], gl.maps[0][3], gl.maps[0][4],
+                         gl.maps[0][1], p, gl);
   if (err != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;

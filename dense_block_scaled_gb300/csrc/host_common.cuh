@@ -64,22 +64,48 @@ inline int raster_group(int block_rows, int k, int fmt, int tiles_m, bool dual =
   return g;
 }
 
-// BF16 dual accumulate (256 x 512 pair tiles) unless the wider tiles fill the
-// waves of CTA pairs clearly worse than 256 x 256 tiles do (2048-row bands of
-// 16384^2: 3.4 waves against 6.7; 2048^3: half a wave); TKG_OPT_BF16_TILE_N
-// forces 256 or 512.
+// The last partial round of tiles is split into half-width tiles when its
+// halves fit one round and at most this many full rounds precede it.  With
+// more, cluster launch control has staggered the clusters enough that the last
+// round is already short (measured at 8192^3: NVFP4 unchanged, MXFP8 2-4%
+// slower split; at 4096^3, 3 full rounds: BF16 +4.8%, MXFP8 +1.8%, NVFP4 +2.3%).
+constexpr int kTailSplitMaxRounds = 4;
+inline bool split_tail(long long tiles, int clusters) {
+  const long long full = tiles / clusters, r = tiles % clusters;
+  return r > 0 && 2 * r <= clusters && full <= kTailSplitMaxRounds;
+}
+
+// Rounds of `tiles` equal tiles on `clusters` resident clusters, in units of
+// one tile's time; a split last round counts as half a round.
+inline double tile_rounds(long long tiles, int clusters, bool tail_split) {
+  const long long full = tiles / clusters, r = tiles % clusters;
+  if (r == 0) return double(full);
+  return double(full) + ((tail_split && split_tail(tiles, clusters)) ? 0.5 : 1.0);
+}
+
+// BF16 dual accumulate (256 x 512 pair tiles) unless 256 x 256 tiles finish
+// sooner: each option's time is its rounds of tiles times the tile width, and
+// dual accumulate does the same work about 2-4% faster (measured: 16384^3
+// 1711 -> 1755 TFLOP/s, 8192^3 1715 -> 1750, and 1895-1914 against 1863-1879
+// for 256-wide tiles with a split tail).  At 16384^3 and 8192^3 that is dual,
+// at 4096^3 256-wide tiles (3.5 rounds with the split tail against 2 rounds of
+// twice the width: 1805 against 1723 TFLOP/s).
+// TKG_OPT_BF16_TILE_N forces 256 or 512.
 inline bool use_dual_bf16(const Problem& pr) {
   const int forced = option(TKG_OPT_BF16_TILE_N);
   if (forced == 512) return true;
   if (forced == 256) return false;
   int sms = 0;
   if (device_sm_count(&sms) != TKG_OK || sms < 2) return false;
-  const double pairs = double(sms / 2);
-  auto filled = [&](int bn) {
-    const double tiles = double(ceil_div(pr.m, 256)) * double(ceil_div(pr.n, bn));
-    return tiles / (double((long long)((tiles + pairs - 1.0) / pairs)) * pairs);
-  };
-  return filled(512) >= filled(256) - 0.02;
+  const int pairs = sms / 2;
+  const bool split = option(TKG_OPT_TAIL_SPLIT) != 1;
+  const long long tm = ceil_div(pr.m, 256);
+  // at most half a wave of 512-wide tiles would all run as 256-wide halves,
+  // which the double-buffered 256-wide kernel runs better (2048^3)
+  if (2 * tm * ceil_div(pr.n, 512) <= pairs) return false;
+  const double t512 = 2.0 * tile_rounds(tm * ceil_div(pr.n, 512), pairs, split) / 1.04;
+  const double t256 = tile_rounds(tm * ceil_div(pr.n, 256), pairs, split);
+  return t512 <= t256;
 }
 
 // ---- tensor maps (tkg_api.cu)
@@ -189,6 +215,15 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, uint32_t(b_box), CU_TENSOR_MAP_SWIZZLE_128B)) !=
       TKG_OK)
     return st;
+  // half tiles (the split last wave): an MMA half as wide, each CTA supplying
+  // half as many B rows (dual accumulate: one of its two N = 256 MMAs and boxes)
+  const int b_cta_rows_half = C::kDual ? C::kBBox : (C::kMmaN / 2) / CG;
+  CUtensorMap tmBh = tmB;
+  const bool can_split = GROUPED == 0 && !narrow;
+  if (can_split && !C::kDual &&
+      (st = encode_2d(&tmBh, vt, pr.B, kdim, b_rows, row_bytes, boxk, uint32_t(b_cta_rows_half),
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
+    return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)
     return st;
@@ -264,9 +299,27 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
       max_clusters = sms;
     }
   }
-  int clusters = max_clusters < p.num_tiles ? max_clusters : p.num_tiles;
   const int cap = option(TKG_OPT_MAX_CLUSTERS);
-  if (cap > 0 && clusters > cap) clusters = cap;
+  const int resident = (SCHED == SCHED_STATIC && cap > 0 && cap < max_clusters) ? cap : max_clusters;
+
+  // Split the last partial wave: with T tiles on P resident clusters the last
+  // round holds r = T mod P tiles and takes as long as a full one; when its
+  // 2r half-width tiles still fit one round, it takes about half as long
+  // (split_tail also asks for few full rounds before it).
+  p.tail_start = p.num_tiles;
+  const int split_opt = option(TKG_OPT_TAIL_SPLIT);
+  if (can_split && split_opt != 1 && p.num_tiles > 0) {
+    if (split_opt == 2)
+      p.tail_start = 0;   // every tile in halves (a test of the half-tile path)
+    else if (split_tail(p.num_tiles, resident))
+      p.tail_start = p.num_tiles - p.num_tiles % resident;
+    p.num_tiles += p.num_tiles - p.tail_start;
+  }
+  p.b_cta_rows_half = b_cta_rows_half;
+  p.tx_half = C::tx_bytes(a_rows, C::kDual ? b_box : b_cta_rows_half);
+  p.idesc_half = C::kDual ? idesc_with_n(C::kIdescBase, mma_n) : idesc_with_n(C::kIdescBase, C::kMmaN / 2);
+
+  int clusters = resident < p.num_tiles ? resident : p.num_tiles;
   // cluster launch control: one cluster per tile; running clusters take over
   // the ones that have not started
   if (SCHED == SCHED_CLC) clusters = p.num_tiles;
@@ -276,7 +329,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   p.tx_bytes = C::tx_bytes(a_rows, C::kDual ? 2 * b_box : b_box);
   p.idesc = idesc_with_n(C::kIdescBase, mma_n);
   p.b_cta_rows = b_cta_rows;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, p, gt);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, tmD, tmBh, p, gt);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return TKG_ERR_CUDA;

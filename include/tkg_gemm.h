@@ -295,9 +295,12 @@ typedef enum {
   TKG_OPT_SPLIT_K = 8,        /* 0: split K across 2-3 CTAs when the output has few 128x128
                                   tiles (skinny M); 1: never; 2, 3: that split whenever valid */
   TKG_OPT_RASTER_GROUP = 9,   /* M-blocks per tile-order band (0: sized from L2 and K) */
-  TKG_OPT_BF16_TILE_N = 10    /* BF16 CTA-pair tile width: 256 (two accumulator buffers) or
+  TKG_OPT_BF16_TILE_N = 10,   /* BF16 CTA-pair tile width: 256 (two accumulator buffers) or
                                   512 (dual accumulate: two N=256 MMAs share each A tile);
                                   0: automatic */
+  TKG_OPT_TAIL_SPLIT = 11     /* plain GEMMs on the persistent kernel: 0 splits the last partial
+                                  wave of tiles into half-width tiles when those still fit one
+                                  wave; 1 never; 2 splits every tile (a test of the half tiles) */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);
