@@ -219,8 +219,11 @@ class Workload:
 def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flush_buf=None):
     """Seconds per launch: W untimed launches, then K timed back to back between
     two events on the launching stream (or one event pair per launch around an
-    explicit L2 flush when l2_mode == 'flush')."""
-    for i in range(warmup):
+    explicit L2 flush when l2_mode == 'flush').  The warm-up covers at least one
+    pass over the rotated input copies, so that the timed launches find every
+    copy's tensor maps already encoded (the headline, whose inputs exceed 3x L2,
+    has one copy)."""
+    for i in range(max(warmup, getattr(w, "groups", 1))):
         w.launch(i, tkg)
     torch.cuda.synchronize()
     if dist is not None:

@@ -97,7 +97,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 // Encoding a tensor map costs about a microsecond, and a GEMM needs up to
-// five; small GEMMs are bound by that host work.  Each thread keeps the maps it
+// five (a GEMM list five per GEMM); small GEMMs are bound by that host work.  Each thread keeps the maps it
 // encoded in a small direct-mapped cache keyed by every encoding argument (a
 // map holds only the address and geometry, never the data).
 namespace {
@@ -118,7 +118,7 @@ struct MapEntry {
   MapKey key;
   CUtensorMap map;
 };
-constexpr int kMapCacheSize = 64;
+constexpr int kMapCacheSize = 256;   // 64 KB per thread
 thread_local MapEntry t_map_cache[kMapCacheSize];
 
 uint32_t key_hash(const MapKey& k) {
