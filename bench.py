@@ -486,6 +486,16 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     t = timed(lambda: tkg.gemm_grouped_bf16(sizes, A, B, D))
     byts = (groups * n * k + total * k) * 2 + total * n * 2
     out["bf16"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    # the same with the group sizes in device memory (capacity = the rows present)
+    sizes_dev = torch.tensor(sizes, dtype=torch.int32, device=dev)
+
+    def dev_sfa(sa, bs):
+        buf = torch.zeros((tkg.grouped_dev_scale_bytes(groups, total, k, bs),), dtype=torch.uint8, device=dev)
+        buf[:sa.numel()] = sa
+        return buf
+
+    t = timed(lambda: tkg.gemm_grouped_dev_bf16(sizes_dev, A, B, D))
+    out["bf16_device_sizes"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
     del A, B
     sfb = tkg.scale_bytes(n, k, 32)
     blk = tkg.scale_bytes(128, k, 32)
@@ -503,6 +513,10 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     t = timed(lambda: tkg.gemm_grouped_mxfp8(sizes, A8, B8, SA8, SB8, D))
     byts = groups * (n * k + sfb) + total * k + SA8.numel() + total * n * 2
     out["mxfp8"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    SA8d = dev_sfa(SA8, 32)
+    t = timed(lambda: tkg.gemm_grouped_dev_mxfp8(sizes_dev, A8, B8, SA8d, SB8, D))
+    out["mxfp8_device_sizes"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    del SA8d
     del A8, SA8, B8, SB8
     # NVFP4: one tensor scale for all of A (the experts' rows quantised together, each group into its own
     # 128-row scale block with the scale of the whole), one per expert for B
@@ -528,6 +542,10 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     t = timed(lambda: tkg.gemm_grouped_nvfp4(sizes, A4, B4, SA4, SB4, D, ta=TA, tb=TB))
     byts = groups * (n * k // 2 + sfb4) + total * k // 2 + SA4.numel() + total * n * 2
     out["nvfp4"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    SA4d = dev_sfa(SA4, 16)
+    t = timed(lambda: tkg.gemm_grouped_dev_nvfp4(sizes_dev, A4, B4, SA4d, SB4, D, ta=TA, tb=TB))
+    out["nvfp4_device_sizes"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / hbm_gbs}
+    del SA4d
     del A4, SA4, B4, SB4, TA, TB, D
     torch.cuda.empty_cache()
     return out

@@ -36,16 +36,28 @@ tkg_status launch_grouped_nvfp4(const Problem& pr, cudaStream_t s) {
 }
 
 // Device-resident group sizes: the shared-memory group table takes 2 KB, so
-// these run one stage fewer than the host-table versions.
+// these run one stage fewer than the host-table versions (MXFP8 single-CTA
+// keeps its 4 stages with one epilogue staging buffer per warp).  Single-CTA tiles when the row
+// capacity is at most 128 (no group can exceed one 128-row tile: the decode
+// regime, as for the host-table launch above).
+static bool grouped_dev_single_cta(const Problem& pr) {
+  const int cg = option(TKG_OPT_CTA_GROUP);
+  if (cg != 0) return cg == 1;
+  return pr.m <= 128;
+}
+
 tkg_status launch_grouped_dev_bf16(const Problem& pr, cudaStream_t s) {
+  if (grouped_dev_single_cta(pr)) return launch_sched<FMT_BF16, 1, 256, 3, 2, 2>(pr, s);
   return launch_sched<FMT_BF16, 2, 256, 5, 2, 2>(pr, s);
 }
 
 tkg_status launch_grouped_dev_mxfp8(const Problem& pr, cudaStream_t s) {
+  if (grouped_dev_single_cta(pr)) return launch_sched<FMT_MXFP8, 1, 256, 4, 1, 2>(pr, s);
   return launch_sched<FMT_MXFP8, 2, 256, 5, 1, 2>(pr, s);
 }
 
 tkg_status launch_grouped_dev_nvfp4(const Problem& pr, cudaStream_t s) {
+  if (grouped_dev_single_cta(pr)) return launch_sched<FMT_NVFP4, 1, 256, 3, 1, 2>(pr, s);
   return launch_sched<FMT_NVFP4, 2, 256, 4, 1, 2>(pr, s);
 }
 

@@ -338,6 +338,8 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   static_assert(GROUPED != 2 || SCHED == SCHED_STATIC, "device group sizes need the static schedule");
+  static_assert(GROUPED != 2 || C::kSmemBytes + (4 * kMaxGroups + 2) * 4 + 16 <= 232448,
+                "dynamic shared memory and the group table exceed an SM's shared memory");
   // GROUPED == 2: first tile, first row, rows and first SFA block of each
   // group, then the tile count
   __shared__ int s_gtab[GROUPED == 2 ? 4 * kMaxGroups + 2 : 1];

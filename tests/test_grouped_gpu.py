@@ -210,6 +210,25 @@ def test_grouped_device_sizes_equal_host_sizes(fmt, sizes):
     assert (out[total:] == GUARD).all()
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_device_sizes_decode_capacity(fmt):
+    # the decode regime with device sizes: 8 groups of 16 rows in a capacity of
+    # 128 rows (single-CTA tiles), bit for bit the host-table launch
+    sizes = [16] * 8
+    n, k = 520, 1024
+    ops = GroupedOperands(fmt, sizes, n, k, seed=3350)
+    dev = ops.upload()
+    D_host = torch.empty((128, n), dtype=torch.bfloat16, device="cuda")
+    run_grouped(fmt, sizes, dev, D_host)
+    dev_c = _with_capacity(fmt, ops, dev, 128)
+    D = torch.full((128, n), GUARD, dtype=torch.int16, device="cuda")
+    run_grouped_dev(fmt, torch.tensor(sizes, dtype=torch.int32, device="cuda"), dev_c, D.view(torch.bfloat16))
+    assert tkg.device_status() == tkg.OK
+    assert torch.equal(D.cpu(), D_host.cpu().view(torch.int16))
+    ref, S = ops.reference()
+    assert_within_tolerance(bf16_to_f64(D_host), ref, S, f"{fmt} decode groups")
+
+
 def test_grouped_device_sizes_negative_and_over_capacity():
     n, k = 136, 256
     ops = GroupedOperands("bf16", [5, 0, 7], n, k, seed=3400)
