@@ -36,6 +36,8 @@ sys.path.insert(0, ROOT)
 PAGES_PEAK_TFLOPS = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 9000.0}   # HGX B200 dense figures the pages list
 NOMINAL_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}                 # GB300 dense fp8/fp4 vs bf16 (4.5, 13.5 vs 2.25 PF)
 SEEDS = {"bf16": 1001, "mxfp8": 1002, "nvfp4": 1003}                      # 1000 + workload index
+PAUSE_S = [0.0]   # idle seconds before each timed workload (set from --sleep-ms after the headline)
+QUEUE_DELAY_CYCLES_PER_STEP = 100000   # ~50 us of GPU delay per queued launch (host issue takes ~15 us)
 
 
 def parse_args():
@@ -68,6 +70,8 @@ def parse_args():
     ap.add_argument("--grouped", default="8,16384,4096,7168",
                     help="grouped GEMM reported beside the headline: groups,total rows,N,K ('' to skip)")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate")
+    ap.add_argument("--sleep-ms", type=int, default=500,
+                    help="idle time before each timed workload after the headline (the pages' method: 500 ms)")
     ap.add_argument("--vendor", default="",
                     help="M=N=K sizes at which the vendor library's GEMMs (cuBLAS / cuBLASLt through torch) are timed "
                          "beside this library's on the same operands, as context (empty: skip)")
@@ -108,7 +112,8 @@ class ClockSampler:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,temperature.gpu")
 
     def __init__(self, device_uuid):
         self.uuid = device_uuid
@@ -138,7 +143,9 @@ class ClockSampler:
             if len(f) < 8:
                 continue
             try:
-                rows.append((float(f[0]), float(f[1]), float(f[2]), f[4:8]))
+                mem = float(f[8]) if len(f) > 8 else float("nan")
+                temp = float(f[9]) if len(f) > 9 else float("nan")
+                rows.append((float(f[0]), float(f[1]), float(f[2]), f[4:8], mem, temp))
             except ValueError:
                 continue
         os.unlink(self.out.name)
@@ -148,6 +155,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "mem_mhz": statistics.median(r[4] for r in loaded), "temp_c_max": max(r[5] for r in rows),
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
 
 
@@ -223,6 +231,9 @@ def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flu
     pass over the rotated input copies, so that the timed launches find every
     copy's tensor maps already encoded (the headline, whose inputs exceed 3x L2,
     has one copy)."""
+    if PAUSE_S[0] > 0:
+        torch.cuda.synchronize()
+        time.sleep(PAUSE_S[0])
     for i in range(max(warmup, getattr(w, "groups", 1))):
         w.launch(i, tkg)
     torch.cuda.synchronize()
@@ -244,6 +255,11 @@ def time_launches(w, steps, warmup, torch, tkg, dist=None, l2_mode="rotate", flu
     else:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        # A short GPU-side delay ahead of the start event (outside the timed
+        # region) lets the host enqueue all K launches before the first one runs,
+        # so launches of ~10 us are timed back to back rather than at the rate
+        # the host issues them; the e2e figure keeps the host's costs.
+        torch.cuda._sleep(QUEUE_DELAY_CYCLES_PER_STEP * min(steps, 400))
         e0.record()
         for i in range(steps):
             w.launch(i, tkg)
@@ -433,6 +449,9 @@ def grouped_timings(formats, groups, total, n, k, steps, warmup, torch, tkg, syn
                 run = lambda: tkg.gemm_grouped_mxfp8(sizes, A, B, SA, SB, D)
             else:
                 run = lambda: tkg.gemm_grouped_nvfp4(sizes, A, B, SA, SB, D, ta=TA, tb=TB)
+        if PAUSE_S[0] > 0:
+            torch.cuda.synchronize()
+            time.sleep(PAUSE_S[0])
         for _ in range(warmup):
             run()
         torch.cuda.synchronize()
@@ -467,6 +486,9 @@ def grouped_decode_timings(groups, rows, n, k, steps, warmup, torch, tkg, synth,
     D = torch.empty((total, n), dtype=torch.bfloat16, device=dev)
 
     def timed(run):
+        if PAUSE_S[0] > 0:
+            torch.cuda.synchronize()
+            time.sleep(PAUSE_S[0])
         for _ in range(warmup):
             run()
         torch.cuda.synchronize()
@@ -862,6 +884,7 @@ def run_ours(args):
                                                 if pk["bf16_sustained"] else None),
                      "frac_of_pages_peak": tf / PAGES_PEAK_TFLOPS[hf]}
 
+    PAUSE_S[0] = max(args.sleep_ms, 0) / 1e3   # from here on every timed workload starts after an idle pause
     vendor_peak = {}   # the vendor library's same-loop TFLOP/s on the same operands: a measured per-format peak
 
     def fmt_entry(w, t):
