@@ -74,6 +74,12 @@ struct GemmParams {
   uint32_t tx_half;          // stage bytes of a half tile
   uint32_t idesc_half;       // its MMA descriptor (N halved; dual accumulate: one of its two MMAs)
   int b_cta_rows_half;       // B rows each CTA supplies to a half tile's MMA
+  // Plain GEMMs: the epilogue writes D from registers with 16-byte stores
+  // (direct_store != 0; rows and columns masked at m and n) instead of staging
+  // 32 x 32 boxes in shared memory for TMA stores.
+  int direct_store;
+  void* d;                   // D (for direct stores)
+  int ldd;                   // its row pitch in elements
 };
 
 template <int FMT>
@@ -880,7 +886,8 @@ __global__ void __launch_bounds__(384, 1)
       const int row0 = tc.a_row + q * 32;
       // a 32-row box that crosses the end of a group (grouped GEMM) is stored
       // row by row so that the next group's rows are left alone
-      const bool masked = (GROUPED == 1 || GROUPED == 2) && row0 + 32 > tc.row_limit;
+      const bool masked = ((GROUPED == 1 || GROUPED == 2) && row0 + 32 > tc.row_limit) ||
+                          (GROUPED == 0 && p.direct_store != 0);
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
       // a half tile holds BN / 2 columns: the warps of the second column half
       // only hand the accumulator back
@@ -919,7 +926,16 @@ __global__ void __launch_bounds__(384, 1)
         if (idle) continue;
         const int col0 = tc.n0 + h * (BN / 2) + pass * 128;
         if (masked) {
-          if constexpr (GROUPED == 1 || GROUPED == 2) {
+          if constexpr (GROUPED != 3) {
+            uint16_t* dbase;
+            size_t ldd;
+            if constexpr (GROUPED == 1 || GROUPED == 2) {
+              dbase = static_cast<uint16_t*>(gt.d);
+              ldd = size_t(gt.ldd);
+            } else {
+              dbase = static_cast<uint16_t*>(p.d);
+              ldd = size_t(p.ldd);
+            }
             const int r = row0 + lane;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -933,8 +949,7 @@ __global__ void __launch_bounds__(384, 1)
                                           __uint_as_float(v[c][8 * j + 2 * x + 1]) * alpha);
                 const int col = col0 + c * 32 + j * 8;
                 if (r < tc.row_limit && col < p.n) {
-                  uint4* dst =
-                      reinterpret_cast<uint4*>(static_cast<uint16_t*>(gt.d) + size_t(r) * size_t(gt.ldd) + col);
+                  uint4* dst = reinterpret_cast<uint4*>(dbase + size_t(r) * ldd + col);
                   *dst = make_uint4(w[0], w[1], w[2], w[3]);
                 }
               }

@@ -123,7 +123,8 @@ tkg_status launch_list(const tkg_gemm_desc* const* gemms, int count, cudaStream_
 
   GemmParams p{};
   p.num_tiles = int(tiles);
-  p.tail_start = p.num_tiles;   // lists keep whole tiles
+  p.tail_start = p.num_tiles;   // lists keep whole tiles and TMA stores
+  p.direct_store = 0;
   p.alpha = 1.0f;
   p.ta = nullptr;
   p.tb = nullptr;

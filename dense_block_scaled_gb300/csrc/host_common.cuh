@@ -316,6 +316,20 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
     p.num_tiles += p.num_tiles - p.tail_start;
   }
   p.b_cta_rows_half = b_cta_rows_half;
+  // Epilogue stores: TMA boxes (1) or 16-byte stores from registers (2); plain
+  // GEMMs only.  Automatic: direct stores for dual accumulate with many tiles per
+  // cluster.  Its single 512-column accumulator drains in two passes and is
+  // released only after the second pass's loads; direct stores do not hold
+  // those loads up behind staging-buffer waits (16384^3, 27 rounds of tiles:
+  // 1766 -> 1790 and 1778 -> 1805 TFLOP/s; 8192^3, 7 rounds: equal).  With one
+  // tile per cluster the final drain is all that counts and TMA stores are
+  // faster (M=1024, N=K=8192: 78.7 against 82.3 us), as they are for every other
+  // tile shape (2048^3 BF16 12%, NVFP4 16384^3 5%).
+  const int store_opt = option(TKG_OPT_EPILOGUE_STORE);
+  const bool many_rounds = p.num_tiles >= 8 * resident;
+  p.direct_store = (GROUPED == 0 && (store_opt == 2 || (store_opt == 0 && C::kDual && many_rounds))) ? 1 : 0;
+  p.d = pr.D;
+  p.ldd = pr.ldd > 0 ? pr.ldd : pr.n;
   p.tx_half = C::tx_bytes(a_rows, C::kDual ? b_box : b_cta_rows_half);
   p.idesc_half = C::kDual ? idesc_with_n(C::kIdescBase, mma_n) : idesc_with_n(C::kIdescBase, C::kMmaN / 2);
 

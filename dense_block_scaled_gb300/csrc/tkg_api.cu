@@ -394,7 +394,7 @@ size_t tkg_scale_bytes(int rows, int k, int block) {
 
 tkg_status tkg_set_option(tkg_option o, int value) {
   const int i = int(o);
-  if (i <= 0 || i > int(TKG_OPT_TAIL_SPLIT) || value < 0) return TKG_ERR_INVALID_ARG;
+  if (i <= 0 || i > int(TKG_OPT_EPILOGUE_STORE) || value < 0) return TKG_ERR_INVALID_ARG;
   if (o == TKG_OPT_CTA_GROUP && value > 2) return TKG_ERR_INVALID_ARG;
   g_opts[i].store(value, std::memory_order_relaxed);
   return TKG_OK;

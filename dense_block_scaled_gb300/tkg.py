@@ -24,6 +24,7 @@ OPT_SPLIT_K = 8
 OPT_RASTER_GROUP = 9
 OPT_BF16_TILE_N = 10
 OPT_TAIL_SPLIT = 11
+OPT_EPILOGUE_STORE = 12
 
 EXPORTS = [
     "tkg_gemm_bf16", "tkg_gemm_mxfp8", "tkg_gemm_nvfp4", "tkg_get_device_status", "tkg_status_string",

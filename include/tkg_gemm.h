@@ -298,9 +298,12 @@ typedef enum {
   TKG_OPT_BF16_TILE_N = 10,   /* BF16 CTA-pair tile width: 256 (two accumulator buffers) or
                                   512 (dual accumulate: two N=256 MMAs share each A tile);
                                   0: automatic */
-  TKG_OPT_TAIL_SPLIT = 11     /* plain GEMMs on the persistent kernel: 0 splits the last partial
+  TKG_OPT_TAIL_SPLIT = 11,    /* plain GEMMs on the persistent kernel: 0 splits the last partial
                                   wave of tiles into half-width tiles when those still fit one
                                   wave; 1 never; 2 splits every tile (a test of the half tiles) */
+  TKG_OPT_EPILOGUE_STORE = 12 /* plain GEMMs on the persistent kernel: how the epilogue writes D;
+                                  1 TMA stores of 32 x 32 boxes staged in shared memory, 2 16-byte
+                                  stores from registers; 0 automatic */
 } tkg_option;
 
 tkg_status tkg_set_option(tkg_option option, int value);

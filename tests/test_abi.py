@@ -66,12 +66,12 @@ def test_options_roundtrip(lib):
     # every option the header declares is settable; the next number is not
     for o in (tkg.OPT_CTA_GROUP, tkg.OPT_SINGLE_STAGE, tkg.OPT_TIMEOUT_MS, tkg.OPT_INJECT_STALL,
               tkg.OPT_MAX_CLUSTERS, tkg.OPT_ACC_STAGES, tkg.OPT_SCHEDULER, tkg.OPT_SPLIT_K,
-              tkg.OPT_RASTER_GROUP, tkg.OPT_BF16_TILE_N, tkg.OPT_TAIL_SPLIT):
+              tkg.OPT_RASTER_GROUP, tkg.OPT_BF16_TILE_N, tkg.OPT_TAIL_SPLIT, tkg.OPT_EPILOGUE_STORE):
         tkg.set_option(o, 1)
         assert tkg.get_option(o) == 1
         tkg.set_option(o, 0)
     with pytest.raises(tkg.TkgError):
-        tkg.set_option(tkg.OPT_TAIL_SPLIT + 1, 0)
+        tkg.set_option(tkg.OPT_EPILOGUE_STORE + 1, 0)
     assert lib.tkg_status_string(5) == b"device wait timed out"
 
 
