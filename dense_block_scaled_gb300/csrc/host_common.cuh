@@ -27,11 +27,16 @@ struct Problem {
   int groups = 0;            // grouped GEMM: number of groups, and their sizes (host)
   const int* m_sizes = nullptr;
   int ldd = 0;               // row stride of D in elements (0: n); plain GEMMs only
+  uint64_t lda_bytes = 0;    // row pitch of A and B in bytes (0: contiguous rows); plain GEMMs only
+  uint64_t ldb_bytes = 0;
   unsigned int* status = nullptr;   // device status word to use (null: the library's, allocated on first use)
 };
 
 // row stride of D in bytes
 inline uint64_t d_row_bytes(const Problem& pr) { return uint64_t(pr.ldd > 0 ? pr.ldd : pr.n) * 2; }
+// row pitches of A and B in bytes, given the contiguous pitch for the format
+inline uint64_t a_row_bytes(const Problem& pr, uint64_t contiguous) { return pr.lda_bytes ? pr.lda_bytes : contiguous; }
+inline uint64_t b_row_bytes(const Problem& pr, uint64_t contiguous) { return pr.ldb_bytes ? pr.ldb_bytes : contiguous; }
 
 // ---- options and per-device state (tkg_api.cu)
 int option(tkg_option o);
@@ -201,8 +206,8 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   // M=1).  A grouped tile starts at its group's first row, so its box may still
   // run past the end, by fewer rows than M.
   const int a_rows = pr.m < C::kCtaM ? pr.m : C::kCtaM;
-  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
-      TKG_OK)
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, a_row_bytes(pr, row_bytes), boxk, uint32_t(a_rows),
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   // Narrow B (N at most half the MMA width; not dual, not grouped): the MMA runs
   // half as wide, each CTA of a pair supplying half its columns, so the tensor
@@ -212,8 +217,8 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   const int mma_n = narrow ? C::kMmaN / 2 : C::kMmaN;
   const int b_cta_rows = C::kDual ? C::kBBox : mma_n / CG;
   const int b_box = (GROUPED == 0 && pr.n < b_cta_rows) ? pr.n : b_cta_rows;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, row_bytes, boxk, uint32_t(b_box), CU_TENSOR_MAP_SWIZZLE_128B)) !=
-      TKG_OK)
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, b_rows, b_row_bytes(pr, row_bytes), boxk, uint32_t(b_box),
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   // half tiles (the split last wave): an MMA half as wide, each CTA supplying
   // half as many B rows (dual accumulate: one of its two N = 256 MMAs and boxes)
@@ -221,7 +226,7 @@ tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
   CUtensorMap tmBh = tmB;
   const bool can_split = GROUPED == 0 && !narrow;
   if (can_split && !C::kDual &&
-      (st = encode_2d(&tmBh, vt, pr.B, kdim, b_rows, row_bytes, boxk, uint32_t(b_cta_rows_half),
+      (st = encode_2d(&tmBh, vt, pr.B, kdim, b_rows, b_row_bytes(pr, row_bytes), boxk, uint32_t(b_cta_rows_half),
                       CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
@@ -373,14 +378,14 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
   const uint32_t boxk = bf16 ? 64 : 128;
   tkg_status st;
   const int a_rows = pr.m < AROWS ? pr.m : AROWS;   // no A box partly past the last row (see launch_gemm)
-  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, row_bytes, boxk, uint32_t(a_rows), CU_TENSOR_MAP_SWIZZLE_128B)) !=
-      TKG_OK)
+  if ((st = encode_2d(&tmA, vt, pr.A, kdim, pr.m, a_row_bytes(pr, row_bytes), boxk, uint32_t(a_rows),
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   // narrow B: an MMA of N = 64 (the tile's 128 columns would be mostly absent), box clipped to N rows
   const int mma_n = pr.n <= C::BN / 2 ? C::BN / 2 : C::BN;
   const int b_box = pr.n < mma_n ? pr.n : mma_n;
-  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, row_bytes, boxk, uint32_t(b_box), CU_TENSOR_MAP_SWIZZLE_128B)) !=
-      TKG_OK)
+  if ((st = encode_2d(&tmB, vt, pr.B, kdim, pr.n, b_row_bytes(pr, row_bytes), boxk, uint32_t(b_box),
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != TKG_OK)
     return st;
   if ((st = encode_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr.D, pr.n, pr.m, d_row_bytes(pr), 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_64B)) != TKG_OK)

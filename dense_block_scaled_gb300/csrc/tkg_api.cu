@@ -248,6 +248,77 @@ tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void* A, const void* B, con
   return launch_nvfp4(pr, stream);
 }
 
+// Row pitches of the strided entry points.  lda / ldb count the operands'
+// storage units (BF16 elements; bytes of E4M3 or packed E2M1 codes), ldd BF16
+// elements of D.  Checks as check_common, plus: a pitch shorter than a row is
+// an invalid argument, a pitch that is not a multiple of 16 bytes a
+// misalignment.  k == 0 zeroes the m x n block of D.
+static tkg_status check_strided(int m, int n, int k, const void* A, int lda, const void* B, int ldb, void* D, int ldd,
+                                int k_multiple, int unit_bytes, int units_per_row, bool* empty, cudaStream_t stream) {
+  *empty = false;
+  if (m < 0 || n < 0 || k < 0 || lda < 0 || ldb < 0 || ldd < 0) return TKG_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) {
+    *empty = true;
+    return TKG_OK;
+  }
+  if (!D || ldd < n) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(D) || (ldd % 8) != 0) return TKG_ERR_ALIGNMENT;
+  if (k == 0) {
+    *empty = true;
+    return cudaMemset2DAsync(D, size_t(ldd) * 2, 0, size_t(n) * 2, size_t(m), stream) == cudaSuccess ? TKG_OK
+                                                                                                     : TKG_ERR_CUDA;
+  }
+  if (!A || !B || lda < units_per_row || ldb < units_per_row) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || (k % k_multiple) != 0 || (size_t(lda) * unit_bytes) % 16 != 0 ||
+      (size_t(ldb) * unit_bytes) % 16 != 0)
+    return TKG_ERR_ALIGNMENT;
+  return TKG_OK;
+}
+
+tkg_status tkg_gemm_bf16_strided(int m, int n, int k, const void* A, int lda, const void* B, int ldb, void* D, int ldd,
+                                 float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_strided(m, n, k, A, lda, B, ldb, D, ldd, 8, 2, k, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  Problem pr{m, n, k, A, B, nullptr, nullptr, nullptr, nullptr, D, alpha};
+  pr.ldd = ldd;
+  pr.lda_bytes = uint64_t(lda) * 2;
+  pr.ldb_bytes = uint64_t(ldb) * 2;
+  return launch_bf16(pr, stream);
+}
+
+tkg_status tkg_gemm_mxfp8_strided(int m, int n, int k, const void* A, int lda, const void* B, int ldb, const void* sfa,
+                                  const void* sfb, void* D, int ldd, float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_strided(m, n, k, A, lda, B, ldb, D, ldd, 32, 1, k, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  Problem pr{m, n, k, A, B, sfa, sfb, nullptr, nullptr, D, alpha};
+  pr.ldd = ldd;
+  pr.lda_bytes = uint64_t(lda);
+  pr.ldb_bytes = uint64_t(ldb);
+  return launch_mxfp8(pr, stream);
+}
+
+tkg_status tkg_gemm_nvfp4_strided(int m, int n, int k, const void* A, int lda, const void* B, int ldb, const void* sfa,
+                                  const void* sfb, const float* tensor_scale_a, const float* tensor_scale_b, void* D,
+                                  int ldd, float alpha, cudaStream_t stream) {
+  bool empty;
+  tkg_status st = check_strided(m, n, k, A, lda, B, ldb, D, ldd, 32, 1, k / 2, &empty, stream);
+  if (st != TKG_OK || empty) return st;
+  if (!sfa || !sfb) return TKG_ERR_INVALID_ARG;
+  if (!aligned16(sfa) || !aligned16(sfb)) return TKG_ERR_ALIGNMENT;
+  if ((tensor_scale_a && (reinterpret_cast<uintptr_t>(tensor_scale_a) & 3u)) ||
+      (tensor_scale_b && (reinterpret_cast<uintptr_t>(tensor_scale_b) & 3u)))
+    return TKG_ERR_ALIGNMENT;
+  Problem pr{m, n, k, A, B, sfa, sfb, tensor_scale_a, tensor_scale_b, D, alpha};
+  pr.ldd = ldd;
+  pr.lda_bytes = uint64_t(lda);
+  pr.ldb_bytes = uint64_t(ldb);
+  return launch_nvfp4(pr, stream);
+}
+
 tkg_status tkg_gemm_grouped_bf16(int groups, const int* m_sizes, int n, int k, const void* A, const void* B, void* D,
                                  float alpha, cudaStream_t stream) {
   bool empty;

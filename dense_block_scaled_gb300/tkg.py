@@ -34,6 +34,7 @@ EXPORTS = [
     "tkg_gemm_bf16_from_host", "tkg_gemm_grouped_dev_bf16", "tkg_gemm_grouped_dev_mxfp8",
     "tkg_gemm_grouped_dev_nvfp4", "tkg_grouped_dev_scale_bytes", "tkg_quantize_nvfp4_scaled",
     "tkg_gemm_list_bf16", "tkg_gemm_list_mxfp8", "tkg_gemm_list_nvfp4",
+    "tkg_gemm_bf16_strided", "tkg_gemm_mxfp8_strided", "tkg_gemm_nvfp4_strided",
 ]
 
 MAX_LIST = 16
@@ -85,6 +86,11 @@ def load() -> ctypes.CDLL:
             lib.tkg_grouped_dev_scale_bytes.restype = ctypes.c_size_t
             for name in ("tkg_gemm_list_bf16", "tkg_gemm_list_mxfp8", "tkg_gemm_list_nvfp4"):
                 getattr(lib, name).argtypes = [i, ctypes.POINTER(GemmDesc), vp]
+                getattr(lib, name).restype = ctypes.c_int
+            lib.tkg_gemm_bf16_strided.argtypes = [i, i, i, vp, i, vp, i, vp, i, f, vp]
+            lib.tkg_gemm_mxfp8_strided.argtypes = [i, i, i, vp, i, vp, i, vp, vp, vp, i, f, vp]
+            lib.tkg_gemm_nvfp4_strided.argtypes = [i, i, i, vp, i, vp, i, vp, vp, vp, vp, vp, i, f, vp]
+            for name in ("tkg_gemm_bf16_strided", "tkg_gemm_mxfp8_strided", "tkg_gemm_nvfp4_strided"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.tkg_get_device_status.argtypes = [vp]
             lib.tkg_status_string.argtypes = [st]
@@ -200,6 +206,23 @@ def gemm_nvfp4(A, B, sfa, sfb, D, alpha: float = 1.0, ta=None, tb=None, stream=N
     n = B.shape[0]
     _check(gemm_nvfp4_raw(m, n, 2 * kh, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb), _ptr(D),
                           alpha, _stream(stream)), "tkg_gemm_nvfp4")
+
+
+def gemm_strided(fmt: str, m: int, n: int, k: int, A, lda: int, B, ldb: int, D, ldd: int, alpha: float = 1.0,
+                 sfa=None, sfb=None, ta=None, tb=None, stream=None) -> None:
+    """The GEMM on row-pitched views: lda / ldb in storage units (bf16 elements, or bytes of E4M3 / packed E2M1
+    codes), ldd in bf16 elements; A, B, D are the first elements of the views."""
+    lib = load()
+    s = _stream(stream)
+    if fmt == "bf16":
+        st = lib.tkg_gemm_bf16_strided(m, n, k, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldd, ctypes.c_float(alpha), s)
+    elif fmt == "mxfp8":
+        st = lib.tkg_gemm_mxfp8_strided(m, n, k, _ptr(A), lda, _ptr(B), ldb, _ptr(sfa), _ptr(sfb), _ptr(D), ldd,
+                                        ctypes.c_float(alpha), s)
+    else:
+        st = lib.tkg_gemm_nvfp4_strided(m, n, k, _ptr(A), lda, _ptr(B), ldb, _ptr(sfa), _ptr(sfb), _ptr(ta), _ptr(tb),
+                                        _ptr(D), ldd, ctypes.c_float(alpha), s)
+    _check(st, f"tkg_gemm_{fmt}_strided")
 
 
 def gemm_grouped_bf16(m_sizes, A, B, D, alpha: float = 1.0, stream=None) -> None:

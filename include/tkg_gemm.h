@@ -87,6 +87,27 @@ tkg_status tkg_gemm_nvfp4(int m, int n, int k, const void *A, const void *B, con
                           const float *tensor_scale_a, const float *tensor_scale_b, void *D, float alpha,
                           cudaStream_t stream);
 
+/* The three GEMMs above on matrices with row pitches (views into larger
+ * buffers, or rows padded for alignment).  Same products, scales and checks,
+ * except that row i of A starts lda units after row i-1 and row j of B ldb
+ * units after row j-1, where a unit is an element of the operand's storage
+ * (a bfloat16 for BF16; a byte, i.e. one E4M3 code or two E2M1 codes, for
+ * MXFP8 and NVFP4), and row i of D starts ldd bfloat16 elements after row i-1.
+ * Requires lda, ldb >= the row length (k, or k/2 bytes for NVFP4) and ldd >= n
+ * (else TKG_ERR_INVALID_ARG), and pitches that are multiples of 16 bytes (else
+ * TKG_ERR_ALIGNMENT); bytes between rows are neither read (A, B) nor written
+ * (D).  k == 0 writes zeros to the m x n block of D.
+ * Pitches that are an odd multiple of 16 bytes start every other row 16 bytes
+ * off a 32-byte boundary, so its 128-byte pieces span five 32-byte sectors
+ * instead of four: such GEMMs run 20-27% slower than with 32-byte multiples. */
+tkg_status tkg_gemm_bf16_strided(int m, int n, int k, const void *A, int lda, const void *B, int ldb, void *D, int ldd,
+                                 float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_mxfp8_strided(int m, int n, int k, const void *A, int lda, const void *B, int ldb, const void *sfa,
+                                  const void *sfb, void *D, int ldd, float alpha, cudaStream_t stream);
+tkg_status tkg_gemm_nvfp4_strided(int m, int n, int k, const void *A, int lda, const void *B, int ldb, const void *sfa,
+                                  const void *sfb, const float *tensor_scale_a, const float *tensor_scale_b, void *D,
+                                  int ldd, float alpha, cudaStream_t stream);
+
 /* Grouped GEMM, the mixture-of-experts form named as work in progress in
  * "ThunderKittens 2.0 GPU Kernel优化" (section after Figure 1: grouped GEMM
  * kernels under development).  The pages give no interface; this one keeps the

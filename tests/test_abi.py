@@ -140,3 +140,14 @@ def test_gemm_list_host_side_checks(lib):
     # empty entries only: nothing to do
     empty = tkg.GemmDesc(0, 64, 64, None, None, None, None, None, None, None, 1.0)
     assert tkg.gemm_list_raw("bf16", [empty, empty], None) == tkg.OK
+
+
+def test_strided_host_side_checks(lib):
+    # pitches shorter than a row, or not a multiple of 16 bytes, are rejected before any CUDA call
+    assert lib.tkg_gemm_bf16_strided(64, 64, 64, 16, 56, 16, 64, 16, 64, 1.0, None) == 1      # lda < k
+    assert lib.tkg_gemm_bf16_strided(64, 64, 64, 16, 68, 16, 64, 16, 64, 1.0, None) == 2      # 136-byte pitch
+    assert lib.tkg_gemm_bf16_strided(64, 64, 64, 16, 64, 16, 64, 16, 60, 1.0, None) == 1      # ldd < n
+    assert lib.tkg_gemm_mxfp8_strided(64, 64, 64, 16, 72, 16, 64, 16, 16, 16, 64, 1.0, None) == 2   # 72 bytes
+    assert lib.tkg_gemm_nvfp4_strided(64, 64, 64, 16, 16, 16, 32, 16, 16, None, None, 16, 64, 1.0, None) == 1  # < k/2
+    assert lib.tkg_gemm_nvfp4_strided(64, 64, 64, 16, 40, 16, 32, 16, 16, None, None, 16, 64, 1.0, None) == 2
+    assert lib.tkg_gemm_bf16_strided(0, 64, 64, None, 0, None, 0, None, 0, 1.0, None) == 0     # empty
