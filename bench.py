@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 PAGES_PEAK_TFLOPS = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 9000.0}   # HGX B200 dense figures the pages list
+PAGES_HBM_GBS = 8000.0                                                     # the HBM bandwidth in the same table
 NOMINAL_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}                 # GB300 dense fp8/fp4 vs bf16 (4.5, 13.5 vs 2.25 PF)
 SEEDS = {"bf16": 1001, "mxfp8": 1002, "nvfp4": 1003}                      # 1000 + workload index
 PAUSE_S = [0.0]   # idle seconds before each timed workload (set from --sleep-ms after the headline)
@@ -777,7 +778,7 @@ def config_table(by_format, nontile, skinny, size, lists=None):
     for key, e in skinny.items():
         out[key.replace("bf16", "BF16").replace("nvfp4", "NVFP4")] = {
             "us": e["us"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
-            "frac_of_roofline": e["frac_of_roofline"]}
+            "frac_of_pages_hbm": e.get("frac_of_pages_hbm"), "frac_of_roofline": e["frac_of_roofline"]}
     for key, e in (lists or {}).items():
         out["list " + key] = {"us_per_gemm": e["us_per_gemm"], "tflops": e["tflops"], "frac_of_hbm": e["frac_of_hbm"],
                               "speedup_vs_single_launches": e.get("speedup_vs_single_launches"),
@@ -961,6 +962,7 @@ def run_ours(args):
                 roof = min(PAGES_PEAK_TFLOPS[fmt], w.flop / byts * pk["hbm_gbs"] / 1e3)
                 skinny[f"{fmt} M={mm} N=K=8192"] = {
                     "us": t * 1e6, "tflops": tf, "gbs": byts / t / 1e9, "frac_of_hbm": byts / t / 1e9 / pk["hbm_gbs"],
+                    "frac_of_pages_hbm": byts / t / 1e9 / PAGES_HBM_GBS,
                     "roofline_tflops": roof, "frac_of_roofline": tf / roof, "input_groups": w.groups,
                     "us_graph": tg * 1e6, "frac_of_roofline_graph": w.flop / tg / 1e12 / roof}
                 del w

@@ -23,6 +23,7 @@ def test_pages_peaks_match_the_spec_table():
     g = _golden("hgx_b200_dense_peaks.txt")
     assert bench.PAGES_PEAK_TFLOPS == {"bf16": g["bf16"] * 1000, "mxfp8": g["fp8"] * 1000,
                                        "nvfp4": g["nvfp4"] * 1000}
+    assert bench.PAGES_HBM_GBS == g["hbm_tbs"] * 1000
 
 
 def test_cpu_oracle_sweep_small_configs():
