@@ -49,7 +49,25 @@
 namespace tkg {
 
 enum : int { FMT_BF16 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2 };
-enum : uint32_t { DEV_ERR_TIMEOUT = 1u };
+enum : uint32_t { DEV_ERR_TIMEOUT = 1u, DEV_ERR_CHECK = 2u };
+
+// Check builds (compiled with TKG_CHECK=1): an invariant that does not hold
+// sets DEV_ERR_CHECK in the status word, and the caller skips the access the
+// invariant guards (a skipped load ends in a bounded wait that runs out); no
+// trap, no assert.  In other builds the check compiles to nothing.
+#ifndef TKG_CHECK
+#define TKG_CHECK 0
+#endif
+__device__ __forceinline__ bool invariant(bool ok, unsigned int* status) {
+#if TKG_CHECK
+  if (!ok) atomicOr(status, DEV_ERR_CHECK);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
 
 struct GemmParams {
   int m, n, k;
@@ -400,6 +418,7 @@ __global__ void __launch_bounds__(384, 1)
   };
 
   constexpr bool kList = GROUPED == 3;
+  auto gt_count = [&]() -> int { if constexpr (GROUPED != 0) return gt.count; else return 1; };
   // tensor maps of the GEMM a tile belongs to (a list) or of the launch
   auto map_a = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][0]; else { (void)e; return &tmA; } };
   auto map_b = [&](int e) -> const void* { if constexpr (kList) return &gt.maps[e][1]; else { (void)e; return &tmB; } };
@@ -683,6 +702,16 @@ __global__ void __launch_bounds__(384, 1)
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
           const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);   // TMA x coordinate (elements)
+          // a tile of this launch, a ring slot, a 16-byte aligned x (TMA's rule)
+          if (!invariant(t < num_tiles && stage < uint32_t(STAGES) && ks >= 0 && ks < nks &&
+                             (kx * (FMT == FMT_BF16 ? 2 : 1)) % 16 == 0 && (GROUPED == 0 || tc.group >= 0),
+                         p.status)) {
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           ptx::tma_load_2d<CG>(stage_a(stage), mA, kx, a_row, fb, pol_a);
           ptx::tma_load_2d<CG>(stage_b(stage), mB, kx, b_row, fb, pol_b);
           if constexpr (C::kDual) {   // second half of the 512-column tile
@@ -759,10 +788,16 @@ __global__ void __launch_bounds__(384, 1)
           }
           const uint64_t adesc = sdesc_sw128(stage_a(stage));
           const uint64_t bdesc = sdesc_sw128(stage_b(stage));
+          // the accumulator columns this stage's MMAs write lie inside the allocation
+          const uint32_t n_mma = ((idesc0 >> 17) & 0x3Fu) << 3;
+          const bool stage_ok = invariant(stage < uint32_t(STAGES) && acc < uint32_t(ACC) &&
+                                              acc * uint32_t(C::kAccCols) + n_mma +
+                                                      ((C::kDual && !half) ? 256u : 0u) <= uint32_t(C::kTmemCols),
+                                          p.status);
 #pragma unroll
           for (int j = 0; j < C::kMmasPerStage; ++j) {
             const int k0 = ks * T::kStageK + j * T::kMmaK;
-            if (k0 >= kk) break;
+            if (k0 >= kk || !stage_ok) break;
             const uint64_t koff = uint64_t((j * 32) >> 4);   // 32 bytes of K per MMA
             const uint32_t accum = (it > 0 || j > 0) ? 1u : 0u;
             if constexpr (FMT == FMT_BF16) {
@@ -778,6 +813,12 @@ __global__ void __launch_bounds__(384, 1)
               // read them: one region per stage (MXFP8: MMA j reads byte j of each
               // word) or per MMA (NVFP4: MMA j reads atom j)
               const int g = (FMT == FMT_NVFP4) ? j : 0;
+              // the scale region lies between the accumulators and the end of the allocation
+              if (!invariant(region < uint32_t(C::kRegions) &&
+                                 uint32_t(C::kScaleBase) + (region + 1u) * uint32_t(C::kRegionCols) <=
+                                     uint32_t(C::kTmemCols),
+                             p.status))
+                break;
               if (FMT == FMT_NVFP4 || j == 0) {
                 const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
                 ptx::tmem_cp_32x128b_x4<CG>(reg, sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));
@@ -890,8 +931,11 @@ __global__ void __launch_bounds__(384, 1)
                           (GROUPED == 0 && p.direct_store != 0);
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * C::kAccCols + h * (BN / 2));
       // a half tile holds BN / 2 columns: the warps of the second column half
-      // only hand the accumulator back
-      const bool idle = tc.half >= 0 && h == 1;
+      // only hand the accumulator back (as does every warp if a check fails)
+      const bool idle = (tc.half >= 0 && h == 1) ||
+                        !invariant(acc < uint32_t(ACC) && acc * uint32_t(C::kAccCols) + uint32_t(BN) <= uint32_t(C::kTmemCols) &&
+                                       t < num_tiles && (!kList || tc.group < gt_count()),
+                                   p.status);
 #pragma unroll
       for (int pass = 0; pass < kPasses; ++pass) {
         const int nch = kWarpChunks - 4 * pass < 4 ? kWarpChunks - 4 * pass : 4;

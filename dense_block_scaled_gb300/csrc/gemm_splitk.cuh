@@ -200,6 +200,16 @@ __global__ void __launch_bounds__(384, 1)
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
+        // a ring slot, a K stage of this launch, a 16-byte aligned x (TMA's rule)
+        if (!invariant(stage < uint32_t(STAGES) && ks >= 0 && ks < p.num_kstages &&
+                           (kx * (FMT == FMT_BF16 ? 2 : 1)) % 16 == 0,
+                       p.status)) {
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         ptx::tma_load_2d<1>(stage_a(stage), &tmA, kx, mb * C::BM, full_bar(stage), pol_a);
         ptx::tma_load_2d<1>(stage_b(stage), &tmB, kx, nb * C::BN, full_bar(stage), pol_b);
         if constexpr (C::kScaled) {
@@ -236,16 +246,24 @@ __global__ void __launch_bounds__(384, 1)
         }
         const uint64_t adesc = sdesc_sw128(stage_a(stage));
         const uint64_t bdesc = sdesc_sw128(stage_b(stage));
+        // the accumulator and the scale region lie inside the allocation
+        const uint32_t n_mma = ((p.idesc >> 17) & 0x3Fu) << 3;
+        const bool stage_ok = invariant(stage < uint32_t(STAGES) && n_mma <= uint32_t(C::kAccCols), p.status);
 #pragma unroll
         for (int j = 0; j < C::kMmasPerStage; ++j) {
           const int k0 = ks * T::kStageK + j * T::kMmaK;
-          if (k0 >= p.k) break;
+          if (k0 >= p.k || !stage_ok) break;
           const uint64_t koff = uint64_t((j * 32) >> 4);
           const uint32_t accum = (ks > ks0 || j > 0) ? 1u : 0u;
           if constexpr (FMT == FMT_BF16) {
             ptx::mma_f16<1>(tmem, adesc + koff, bdesc + koff, p.idesc, accum);
           } else {
             const int g = (FMT == FMT_NVFP4) ? j : 0;
+            if (!invariant(region < uint32_t(C::kRegions) &&
+                               uint32_t(C::kScaleBase) + (region + 1u) * uint32_t(C::kRegionCols) <=
+                                   uint32_t(C::kTmemCols),
+                           p.status))
+              break;
             const uint32_t reg = tmem + uint32_t(C::kScaleBase + region * C::kRegionCols);
             if (FMT == FMT_NVFP4 || j == 0) {
               ptx::tmem_cp_32x128b_x4<1>(reg, sdesc_sf(stage_sfa(stage) + uint32_t(512 * g)));

@@ -441,7 +441,8 @@ tkg_status tkg_get_device_status(cudaStream_t stream) {
   if (noalloc_take_status(stream, &h2) != TKG_OK) return TKG_ERR_CUDA;
   h |= h2;
   if (h == 0) return TKG_OK;
-  return (h & DEV_ERR_TIMEOUT) ? TKG_ERR_TIMEOUT : TKG_ERR_CUDA;
+  if (h & DEV_ERR_TIMEOUT) return TKG_ERR_TIMEOUT;
+  return (h & DEV_ERR_CHECK) ? TKG_ERR_CHECK : TKG_ERR_CUDA;
 }
 
 const char* tkg_status_string(tkg_status s) {
@@ -452,6 +453,7 @@ const char* tkg_status_string(tkg_status s) {
     case TKG_ERR_UNSUPPORTED: return "unsupported shape";
     case TKG_ERR_CUDA: return "CUDA error";
     case TKG_ERR_TIMEOUT: return "device wait timed out";
+    case TKG_ERR_CHECK: return "internal check failed";
   }
   return "unknown status";
 }

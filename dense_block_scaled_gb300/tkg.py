@@ -15,9 +15,10 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libtkg.so")
+# TKG_LIBRARY selects another build of the library, e.g. libtkg_check.so
+LIB_PATH = os.environ.get("TKG_LIBRARY") or os.path.join(PKG, "libtkg.so")
 
-OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_CHECK = range(7)
 OPT_CTA_GROUP, OPT_SINGLE_STAGE, OPT_TIMEOUT_MS, OPT_INJECT_STALL, OPT_MAX_CLUSTERS, OPT_ACC_STAGES = 1, 2, 3, 4, 5, 6
 OPT_SCHEDULER = 7
 OPT_SPLIT_K = 8

@@ -56,7 +56,8 @@ typedef enum {
   TKG_ERR_ALIGNMENT = 2,
   TKG_ERR_UNSUPPORTED = 3,
   TKG_ERR_CUDA = 4,
-  TKG_ERR_TIMEOUT = 5
+  TKG_ERR_TIMEOUT = 5,
+  TKG_ERR_CHECK = 6   /* an internal invariant failed in a check build (libtkg_check.so) */
 } tkg_status;
 
 /* BF16 GEMM ("ThunderKittens 2.0", opening section: BF16 GEMM on B200).
@@ -249,12 +250,20 @@ tkg_status tkg_gemm_bf16_from_host(int m, int n, int k, const void *A_host, cons
 tkg_status tkg_gemm_bf16_noalloc(int m, int n, int k, const void *A, const void *B, void *D, float alpha,
                                  cudaStream_t stream);
 
-/* Synchronises `stream`, then reads and clears the current device's status
+/* Check builds.  `python -m dense_block_scaled_gb300.build --check` builds the
+ * same library as libtkg_check.so with every kernel verifying its internal
+ * invariants (tensor-memory column ranges of each MMA, scale copy and
+ * accumulator load; ring-slot, accumulator, tile, group and GEMM-list
+ * indices; the 16-byte alignment of TMA x coordinates).  A failed invariant
+ * skips the access it guards and is reported by tkg_get_device_status as
+ * TKG_ERR_CHECK; nothing traps.  Meant for testing, not for speed.
+ *
+ * Synchronises `stream`, then reads and clears the current device's status
  * words: the library's own (created by the first allocating entry point on the
  * device) and that of tkg_gemm_bf16_noalloc (once set up on the device).
  * Returns TKG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
- * call (its output is then unspecified), TKG_ERR_CUDA on a CUDA error, TKG_OK
- * otherwise.  Allocates nothing: a word that does not exist yet reads as
+ * call (its output is then unspecified), TKG_ERR_CHECK if an invariant failed
+ * (check builds), TKG_ERR_CUDA on a CUDA error, TKG_OK otherwise.  Allocates nothing: a word that does not exist yet reads as
  * clear. */
 tkg_status tkg_get_device_status(cudaStream_t stream);
 

@@ -73,6 +73,7 @@ def test_options_roundtrip(lib):
     with pytest.raises(tkg.TkgError):
         tkg.set_option(tkg.OPT_EPILOGUE_STORE + 1, 0)
     assert lib.tkg_status_string(5) == b"device wait timed out"
+    assert lib.tkg_status_string(6) == b"internal check failed"
 
 
 def test_library_is_sm103a_only():
@@ -151,3 +152,14 @@ def test_strided_host_side_checks(lib):
     assert lib.tkg_gemm_nvfp4_strided(64, 64, 64, 16, 16, 16, 32, 16, 16, None, None, 16, 64, 1.0, None) == 1  # < k/2
     assert lib.tkg_gemm_nvfp4_strided(64, 64, 64, 16, 40, 16, 32, 16, 16, None, None, 16, 64, 1.0, None) == 2
     assert lib.tkg_gemm_bf16_strided(0, 64, 64, None, 0, None, 0, None, 0, 1.0, None) == 0     # empty
+
+
+def test_check_build_compiles_with_the_same_exports():
+    # the check build (kernels verifying their invariants) builds and exports every declared symbol
+    import ctypes
+    from dense_block_scaled_gb300 import build
+    path = build.build(check=True)
+    assert path.endswith("libtkg_check.so")
+    check = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(check, name), name
