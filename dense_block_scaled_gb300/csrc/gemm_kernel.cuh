@@ -147,7 +147,8 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
   return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t(128 >> 4) << 32) | (1ull << 46);
 }
 
-// Tile order: bands of `group` M-blocks walked N-fastest-within-band, so the
+// Tile order: bands of `group` M-blocks; within a band consecutive tiles step
+// through its M-blocks for one N-block, then move to the next N-block, so the
 // clusters running together share A rows and B columns in L2, and a band's A
 // panels stay in L2 while B streams past (the host sizes the band from the L2
 // capacity and the panel size).
