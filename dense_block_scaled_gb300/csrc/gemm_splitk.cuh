@@ -141,7 +141,10 @@ __global__ void __launch_bounds__(384, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (SPLIT > 1) ptx::cluster_sync();
+  // barrier initialisations are published by fence.mbarrier_init (release,
+  // cluster scope), so the arrive is relaxed; the abort flag a peer may write
+  // is written only after a wait has run out its time limit
+  if (SPLIT > 1) ptx::cluster_sync_relaxed();
   ptx::tc_fence_after();
   const uint32_t tmem = s_tmem_base;
 
