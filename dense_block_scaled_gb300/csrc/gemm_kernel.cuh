@@ -551,8 +551,17 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   }
   // Programmatic dependent launch: the set-up above overlapped the previous
-  // kernel's tail; global memory is read only after it has completed.
-  ptx::pdl_wait();
+  // kernel's tail.  Only the roles that read global memory, or hand out work,
+  // wait for the previous grid to complete (griddepcontrol.wait): the producer
+  // right before its first load, the epilogue before it reads the tensor
+  // scales, the scheduler before it takes tiles of clusters not yet launched
+  // (before the release only the clusters resident early would get them).
+  // The MMA issuer touches only shared and tensor memory, and every store of D
+  // follows the producer's first load (through the stage and accumulator
+  // barriers), hence the previous grid's completion.  The producer's set-up
+  // runs before its wait (0.1-0.25 us per launch on 2048^3 and 4096^3 GEMMs).
+  // Device-side group sizes are read by the whole CTA: it waits here.
+  if constexpr (GROUPED == 2) ptx::pdl_wait();
 
   int num_tiles = p.num_tiles;
   if constexpr (GROUPED == 2) {
@@ -671,6 +680,7 @@ __global__ void __launch_bounds__(384, 1)
       // barrier the operand loads complete on: the pair leader's full barrier
       const uint32_t lead_full0 = (CG == 2) ? ptx::map_to_rank(full_bar(0), 0) : full_bar(0);
       uint32_t stage = 0, phase = 0;
+      bool waited = GROUPED == 2;  // past griddepcontrol.wait
       uint32_t armed = 0;          // stages whose last arming is not yet known complete
       uint32_t armed_par = 0;      // parity of that arming
       bool ok = true;
@@ -718,6 +728,10 @@ __global__ void __launch_bounds__(384, 1)
               phase ^= 1u;
             }
             continue;
+          }
+          if (!waited) {
+            ptx::pdl_wait();
+            waited = true;
           }
           ptx::tma_load_2d<CG>(stage_a(stage), mA, kx, a_row, fb, pol_a);
           ptx::tma_load_2d<CG>(stage_b(stage), mB, kx, b_row, fb, pol_b);
@@ -887,6 +901,7 @@ __global__ void __launch_bounds__(384, 1)
   // ------------------------------------------------------------------ tile scheduler
   else if (warp == 2) {
     if constexpr (C::kClc) {
+      if constexpr (GROUPED != 2) ptx::pdl_wait();
       if (leader && ptx::elect_one()) {
         uint32_t slot = 0, ph = 0;
 #pragma unroll 1
@@ -920,6 +935,7 @@ __global__ void __launch_bounds__(384, 1)
     constexpr int kPasses = (kWarpChunks + 3) / 4;     // four chunks (128 registers) per pass
     const uint32_t my_buf0 = epi_base + uint32_t(e * C::kEpiBufs * C::kEpiBufBytes);
     const uint32_t acce_lead0 = (CG == 2) ? ptx::map_to_rank(acce_bar(0), 0) : acce_bar(0);
+    if constexpr (GROUPED != 2) ptx::pdl_wait();
     float alpha0 = p.alpha;
     if (p.ta) alpha0 = alpha0 * __ldg(p.ta);
     if (p.tb) alpha0 = alpha0 * __ldg(p.tb);

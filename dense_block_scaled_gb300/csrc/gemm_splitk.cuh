@@ -175,8 +175,11 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   }
   // Programmatic dependent launch: the set-up above overlapped the previous
-  // kernel's tail; global memory is read only after it has completed.
-  ptx::pdl_wait();
+  // kernel's tail.  Only the roles that read global memory wait for the
+  // previous grid to complete (griddepcontrol.wait): the producer right before
+  // its first load and the storing epilogue before it reads the tensor scales.
+  // The MMA issuer and the partial exchange touch only shared and tensor
+  // memory, and every store of D follows the producer's first load.
 
   Ctl ctl;
   ctl.abort_flag = &s_abort;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t pol_a = ptx::policy_evict_last();    // A is read by every N tile
       const uint64_t pol_b = ptx::policy_evict_first();   // B is read once
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
 #pragma unroll 1
       for (int ks = ks0; ks < ks1; ++ks) {
         if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, ctl)) {
@@ -212,6 +215,10 @@ __global__ void __launch_bounds__(384, 1)
             phase ^= 1u;
           }
           continue;
+        }
+        if (!waited) {
+          ptx::pdl_wait();
+          waited = true;
         }
         ptx::tma_load_2d<1>(stage_a(stage), &tmA, kx, mb * C::BM, full_bar(stage), pol_a);
         ptx::tma_load_2d<1>(stage_b(stage), &tmB, kx, nb * C::BN, full_bar(stage), pol_b);
@@ -388,6 +395,7 @@ __global__ void __launch_bounds__(384, 1)
 
   // ------------------------------------------------------------------ epilogue: the owner stores D
   if (epi && mine && have && !s_abort) {
+    ptx::pdl_wait();
     float alpha = p.alpha;
     if (p.ta) alpha = alpha * __ldg(p.ta);
     if (p.tb) alpha = alpha * __ldg(p.tb);
