@@ -12,12 +12,13 @@ tkg_status launch_bf16(const Problem& pr, cudaStream_t s) {
   // few output tiles (skinny M): split K across a cluster
   const int split = choose_split(pr, FmtTraits<FMT_BF16>::kStageK);
   if (split >= 2 && pr.m <= 32) {
-    // short A tiles leave room for a deeper B pipeline
+    // short A tiles leave room for a deeper B pipeline (the deepest that fits,
+    // 11 stages, ran 0.5-1.6% slower at M = 1 and 16)
     if (split == 2) return launch_splitk<FMT_BF16, 2, 9, 32>(pr, s);
     return launch_splitk<FMT_BF16, 3, 9, 32>(pr, s);
   }
-  if (split == 2) return launch_splitk<FMT_BF16, 2, 6>(pr, s);
-  if (split == 3) return launch_splitk<FMT_BF16, 3, 6>(pr, s);
+  if (split == 2) return launch_splitk<FMT_BF16, 2, 7>(pr, s);
+  if (split == 3) return launch_splitk<FMT_BF16, 3, 7>(pr, s);
   if (option(TKG_OPT_SINGLE_STAGE)) return launch_sched<FMT_BF16, 2, 256, 1, 2>(pr, s);
   if (cg != 1 && option(TKG_OPT_ACC_STAGES) != 1 && use_dual_bf16(pr))
     return launch_sched<FMT_BF16, 2, 512, 4, 1>(pr, s);

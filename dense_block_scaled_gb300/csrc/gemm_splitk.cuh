@@ -53,8 +53,12 @@ struct SplitKConfig {
   static constexpr int kEpiBufBytes = 32 * 64;
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kPartialBytes = BM * BN * 4;   // one CTA's FP32 accumulator
+  // D's staging boxes live in the stage buffers, past the partials that land in
+  // this CTA: by the store every stage load has been consumed.  The 32 KB that
+  // a separate staging area took went to deeper rings.
+  static constexpr int kEpiOffset = (SPLIT - 1) * kPartialBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
-  static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;
   // bytes per stage for A boxes of a_rows rows (at most AROWS) and B boxes of b_rows rows (at most BN)
   static constexpr uint32_t tx_bytes(int a_rows, int b_rows) {
@@ -70,7 +74,8 @@ struct SplitKConfig {
   static_assert(AROWS == 128 || AROWS == 32, "A tile height");
   // the MMA's 128-row read of a short A tile stays inside its stage
   static_assert(BM * kRowBytes <= kStageBytes, "A read past the stage");
-  static_assert((SPLIT - 1) * kPartialBytes <= STAGES * kStageBytes, "partials must fit the stage buffers");
+  static_assert(kEpiOffset + kEpiBytes <= STAGES * kStageBytes,
+                "partials and D's staging boxes must fit the stage buffers");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static constexpr uint32_t kIdesc =
       FMT == FMT_BF16 ? idesc_f16(BM, BN)
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(384, 1)
   auto stage_sfb = [&](int s) {
     return base + uint32_t(s * C::kStageBytes + C::kABytes + C::kBBytes + C::kSfaBytes);
   };
-  const uint32_t epi_base = base + uint32_t(STAGES * C::kStageBytes);
+  const uint32_t epi_base = base + uint32_t(C::kEpiOffset);   // D's staging boxes (stage buffers, past the partials)
   const uint32_t bars = base + uint32_t(C::kBarOffset);
   auto full_bar = [&](int s) { return bars + uint32_t(8 * s); };
   auto empty_bar = [&](int s) { return bars + uint32_t(8 * (STAGES + s)); };

@@ -47,6 +47,9 @@ unsigned int* existing_status_word();                // the current device's wor
 tkg_status noalloc_take_status(cudaStream_t stream, unsigned int* out);
 tkg_status device_sm_count(int* out);
 tkg_status device_l2_bytes(int* out);
+// clusters of `size` (2 or 3) CTAs that can be resident at once when each CTA
+// takes more than half of an SM's shared memory
+tkg_status device_max_clusters(int size, int* out);
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -452,7 +455,10 @@ tkg_status launch_splitk(const Problem& pr, cudaStream_t stream) {
 
 // K split for problems with few 128 x 128 output tiles: 2 or 3 CTAs per tile
 // when that still fits one wave, 0 to use the persistent kernel.  Every CTA's
-// stretch of K (ceil(stages / split) stages) must be non-empty.
+// stretch of K (ceil(stages / split) stages) must be non-empty, and the tiles'
+// clusters must all be resident at once: SMs group into GPCs, so fewer clusters
+// of 3 fit than a third of the SMs (M=16, N=6400, K=8192: 50 clusters of 3 ran
+// in two waves, twice as long as 50 clusters of 2).
 inline int choose_split(const Problem& pr, int stage_k) {
   const int forced = option(TKG_OPT_SPLIT_K);
   if (forced == 1) return 0;
@@ -462,6 +468,13 @@ inline int choose_split(const Problem& pr, int stage_k) {
   const int stages = ceil_div(pr.k, stage_k);
   int split = forced >= 2 ? forced : (tiles * 2 <= sms ? (sms / tiles < 3 ? sms / tiles : 3) : 0);
   while (split >= 2 && (split - 1) * ceil_div(stages, split) >= stages) --split;
+  if (forced < 2) {
+    while (split >= 2) {
+      int fit = 0;
+      if (device_max_clusters(split, &fit) != TKG_OK || tiles <= fit) break;
+      --split;
+    }
+  }
   return split >= 2 ? split : 0;
 }
 

@@ -24,6 +24,7 @@ static std::mutex g_dev_mu;
 static unsigned int* g_status[64] = {};
 static int g_sms[64] = {};
 static int g_l2[64] = {};
+static int g_clusters[64][4] = {};   // resident clusters of 2 and 3 one-per-SM CTAs
 
 static int current_device() {
   int dev = -1;
@@ -62,6 +63,46 @@ tkg_status device_sm_count(int* out) {
     g_sms[dev] = n;
   }
   *out = g_sms[dev];
+  return TKG_OK;
+}
+
+// Stands in for any kernel whose CTAs each take more than half of an SM's
+// shared memory (one CTA per SM): how many clusters of such CTAs can be resident
+// at once depends only on the cluster size and how the SMs group into GPCs.
+static __global__ void __launch_bounds__(384, 1) cluster_capacity_probe() {}
+
+tkg_status device_max_clusters(int size, int* out) {
+  const int dev = current_device();
+  if (dev < 0 || size < 2 || size > 3) return TKG_ERR_CUDA;
+  if (g_clusters[dev][size] == 0) {
+    int sms = 0;
+    tkg_status st = device_sm_count(&sms);
+    if (st != TKG_OK) return st;
+    constexpr int kSmem = 160 * 1024;   // above half of an SM's 228 KB
+    if (cudaFuncSetAttribute(cluster_capacity_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(size);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(size * (sms / size)), 1, 1);
+    cfg.blockDim = dim3(384, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, cluster_capacity_probe, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return TKG_ERR_CUDA;
+    }
+    g_clusters[dev][size] = n;
+  }
+  *out = g_clusters[dev][size];
   return TKG_OK;
 }
 
