@@ -229,16 +229,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
   }
 }
 
-// Shared memory of this CTA -> shared memory of a CTA in the cluster (async
-// proxy), completion counted on `bar` in the destination CTA.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                     uint32_t bar_cluster) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst_cluster),
-               "r"(src), "r"(bytes), "r"(bar_cluster)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
                "r"(src), "r"(x), "r"(y)
