@@ -171,6 +171,9 @@ enum : int { SCHED_STATIC = 0, SCHED_CLC = 1 };
 // start on a 128-row block of their own: SFA block sfa_block0[g], SFB block
 // g * n_blocks.
 constexpr int kMaxGroups = 128;
+// static shared memory of the table a launch with device-resident group sizes
+// builds (first tile, first row, rows and first SFA block per group, the tile count)
+constexpr int kDevGroupTableBytes = (4 * kMaxGroups + 2) * 4 + 16;
 struct GroupTable {
   int count;
   int n_blocks;                       // 128-row scale blocks per group of B
@@ -239,7 +242,9 @@ struct TileCoord {
   int group;
 };
 
-template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC>
+// EXTRA_SMEM: static shared memory the kernel takes besides this layout (the
+// device-size group table), counted when choosing the epilogue staging buffers.
+template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED = SCHED_STATIC, int EXTRA_SMEM = 0>
 struct GemmConfig {
   using T = FmtTraits<FMT>;
   static constexpr bool kScaled = FMT != FMT_BF16;
@@ -274,7 +279,7 @@ struct GemmConfig {
   static constexpr int kClcConsumers = CG * (1 + kEpiWarps) + 2;
   // two staging buffers per epilogue warp when they fit, else one
   static constexpr int kEpiBufs =
-      STAGES * kStageBytes + kEpiWarps * 2 * kEpiBufBytes + kFixedBytes <= 232448 ? 2 : 1;
+      STAGES * kStageBytes + kEpiWarps * 2 * kEpiBufBytes + kFixedBytes + EXTRA_SMEM <= 232448 ? 2 : 1;
   static constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes + kEpiBytes;
   static constexpr int kSmemBytes = kBarOffset + kFixedBytes;
@@ -357,13 +362,13 @@ __global__ void __launch_bounds__(384, 1)
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmBh, const GemmParams p,
                 const __grid_constant__ GroupArg<GROUPED> gt) {
-  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED, GROUPED == 2 ? kDevGroupTableBytes : 0>;
   using T = FmtTraits<FMT>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   static_assert(GROUPED != 2 || SCHED == SCHED_STATIC, "device group sizes need the static schedule");
-  static_assert(GROUPED != 2 || C::kSmemBytes + (4 * kMaxGroups + 2) * 4 + 16 <= 232448,
+  static_assert(GROUPED != 2 || C::kSmemBytes + kDevGroupTableBytes <= 232448,
                 "dynamic shared memory and the group table exceed an SM's shared memory");
   // GROUPED == 2: first tile, first row, rows and first SFA block of each
   // group, then the tile count

@@ -128,7 +128,7 @@ tkg_status encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
 // grouped GEMM over pr.groups groups of rows).
 template <int FMT, int CG, int BN, int STAGES, int ACC, int SCHED, int GROUPED = 0>
 tkg_status launch_gemm(const Problem& pr, cudaStream_t stream) {
-  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED>;
+  using C = GemmConfig<FMT, CG, BN, STAGES, ACC, SCHED, GROUPED == 2 ? kDevGroupTableBytes : 0>;
   using T = FmtTraits<FMT>;
   auto kern = gemm_kernel<FMT, CG, BN, STAGES, ACC, SCHED, GROUPED>;
   // Request at least just over half an SM's shared memory so that no two CTAs
