@@ -74,6 +74,15 @@ def test_split_k_matches_oracle(fmt, shape, split):
     _check(fmt, m, n, k, seed=2000 + m + n + k, alpha=0.5, split=split)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n", [4864, 6400])
+def test_split_choice_by_resident_clusters(fmt, n):
+    # 38 and 50 tiles of 128 columns: 3 CTAs per tile would fit the SMs, but
+    # the automatic choice takes the split only if all its clusters can be
+    # resident at once (50 clusters of 3 cannot); both must match the oracle
+    _check(fmt, 16, n, 2048, seed=2100 + n, alpha=0.5, split=0)
+
+
 @pytest.mark.parametrize("split", [0, 1])
 @pytest.mark.parametrize("m", [1, 2, 7, 8, 9, 31, 100])
 @pytest.mark.parametrize("fmt", FMTS)
