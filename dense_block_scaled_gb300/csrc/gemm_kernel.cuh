@@ -551,6 +551,31 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tma_prefetch_2d(map_b(tc.group), kx, tc.b_row);
       }
     }
+    if constexpr (GROUPED == 2) {
+      // The group sizes may only be read after the dependency wait.  Prefetch
+      // the B tile (and its scales) this cluster's first tile has when every
+      // group holds one row block, the decode regime; a wrong guess costs only
+      // L2 bandwidth (8 experts x 16 rows, N=4096, K=7168: 1.3-1.8 us less).
+      if (ptx::elect_one()) {
+        const int t = int(blockIdx.x) / CG;
+        const int g = t / p.tiles_n;
+        if (g < gt.count) {
+          const int nb = t - g * p.tiles_n;
+          const int b_row = g * p.n + nb * BN + int(rank) * p.b_cta_rows;
+          const int npf = min(p.num_kstages, STAGES);
+#pragma unroll 1
+          for (int ks = 0; ks < npf; ++ks) {
+            const int kx = ks * C::kRowBytes / (FMT == FMT_BF16 ? 2 : 1);
+            ptx::tma_prefetch_2d(&tmB, kx, b_row);
+            if constexpr (C::kScaled) {
+#pragma unroll
+              for (int a = 0; a < C::kSfbBlocks; ++a)
+                ptx::tma_prefetch_3d(&tmSFB, 0, ks * T::kSfAtoms, g * gt.n_blocks + (nb * BN) / 128 + a);
+            }
+          }
+        }
+      }
+    }
     __syncwarp();
   }
   // Programmatic dependent launch: the set-up above overlapped the previous
