@@ -35,3 +35,29 @@ def test_cpu_oracle_sweep_small_configs():
     assert set(out) == {"bf16", "mxfp8", "nvfp4"}
     for label, rows in (("bf16", 64), ("mxfp8", 16), ("nvfp4", 8)):
         assert out[label]["rows"] == rows and out[label]["gflops"] > 0 and out[label]["seconds"] > 0
+
+
+def test_kernel_hash_ignores_comments_only():
+    # recorded counters stay valid across comment edits, not across code edits
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f() { return 1; }  // one\n/* a block\n   comment */\n\nint g();\n"
+    b = "int f() { return 1; }  // other words\n\nint g();\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(a.replace("return 1", "return 2"))
+
+
+def test_recorded_traffic_needs_the_current_kernel_hash(monkeypatch, tmp_path):
+    # roofline.traffic comes from a capture only while the kernel sources are the captured ones
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = {"BF16 GEMM M=N=K=16384": {"dram_bytes_per_launch": 123.0, "kernel_hash": "abc"}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_hash", lambda: "abc")
+    assert bench.recorded_traffic("BF16 GEMM M=N=K=16384") == 123.0
+    assert bench.recorded_traffic("NVFP4 GEMM M=N=K=16384") is None
+    monkeypatch.setattr(bench, "kernel_hash", lambda: "def")
+    assert bench.recorded_traffic("BF16 GEMM M=N=K=16384") is None
