@@ -323,7 +323,8 @@ typedef enum {
                                   clusters take over pending ones); 1: static persistent
                                   grid (TKG_OPT_MAX_CLUSTERS applies only here) */
   TKG_OPT_SPLIT_K = 8,        /* 0: split K across 2-3 CTAs when the output has few 128x128
-                                  tiles (skinny M); 1: never; 2, 3: that split whenever valid */
+                                  tiles (skinny M) and all their clusters can be resident at
+                                  once; 1: never; 2, 3: that split whenever valid */
   TKG_OPT_RASTER_GROUP = 9,   /* M-blocks per tile-order band (0: sized from L2 and K) */
   TKG_OPT_BF16_TILE_N = 10,   /* BF16 CTA-pair tile width: 256 (two accumulator buffers) or
                                   512 (dual accumulate: two N=256 MMAs share each A tile);
