@@ -18,6 +18,12 @@
  *  - Calls are asynchronous on `stream` and return after enqueueing work.
  *    Device-side failures (a bounded wait that ran out) are reported by
  *    tkg_get_device_status().
+ *  - Stream order holds as for any kernel: a GEMM reads what earlier work on
+ *    the stream wrote, and later work sees its D.  GEMM launches carry the
+ *    programmatic-dependent-launch attribute, so a GEMM's set-up (and L2
+ *    prefetches of its first operand tiles) may start while the previous
+ *    kernel finishes; every read of operands, scales and tensor scales, and
+ *    every store of D, waits for that kernel to complete.
  *  - Arguments are checked before anything is launched: negative sizes or a
  *    null pointer give TKG_ERR_INVALID_ARG, a base address or row pitch that
  *    is not a multiple of 16 bytes gives TKG_ERR_ALIGNMENT, shapes the kernels
