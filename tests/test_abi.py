@@ -163,3 +163,19 @@ def test_check_build_compiles_with_the_same_exports():
     check = ctypes.CDLL(path)
     for name in _declared():
         assert hasattr(check, name), name
+
+
+def test_no_multicast_tensor_loads_in_the_sources():
+    # the kernels run as replicas on several GPUs (bench --gpus N): no TMA load
+    # or copy may multicast tensor data across a cluster.  The multicast forms
+    # that move no tensor data (the commit's barrier arrive, the cluster launch
+    # control answer) are allowed.
+    import re
+    csrc = os.path.join(ROOT, "dense_block_scaled_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        for line in text.splitlines():
+            if "multicast" not in line or line.strip().startswith("//"):
+                continue
+            assert re.search(r"tcgen05\.commit|clusterlaunchcontrol\.try_cancel", line), (name, line.strip())
+            assert "cp.async.bulk" not in line, (name, line.strip())
